@@ -1,0 +1,506 @@
+"""Benchmark: paged MLA decode over an FP8 E4M3 KV cache on GB300.
+
+Workload (seeded, synthetic; stands in for the pages' live serving traffic):
+the full decode step at batch 40 -- 78 layers, each with its own pool of
+495,552 x 576 E4M3 slots, 16 heads, contexts uniform in [1024, 8192] plus the
+token appended this step (page size 1).  Per layer: kv_store_fp8 of the new
+token's latent, then mla_decode_run.  All 78 pools (22.3 GB) stay resident;
+one step touches ~8.4 GB of cache, far more than L2, so every layer's rows
+come from HBM.
+
+Reported (one JSON line from rank 0):
+  value         microseconds per MLA FP8 decode call (mla_decode_run over one
+                layer, batch 40), from K passes over the 78 layers
+  ms_per_step   the whole decode step (host plan + 78 x (store + decode))
+  roofline      the decode call's algorithmic bytes / its time vs measured HBM
+  e2e           the same per-call time with the step's inputs copied from
+                pinned host memory and the outputs read back, per layer-call
+  baselines     per decode step: full-pool cast + BF16 decode, and
+                gather-then-cast + BF16 decode
+  cpu_baseline  the CPU oracle on one layer's call, all host cores
+`--impl reference` times the CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+from mla_decode_attention_run_gb300 import accounting as A  # noqa: E402
+
+METRIC = "MLA FP8 decode µs/call & achieved HBM GB/s vs ~8 TB/s peak; decode step ms"
+HEADS, PAGE = 16, 1
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["decode.cu", "common.cuh", "plan.h"]
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, dist=None, device=None) -> float:
+    """Max of a float over all ranks (the slowest replica sets the time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist=None):
+    if dist is not None:
+        dist.barrier()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "mla_decode_attention_run_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, only if
+    it was taken on the current decode kernel source."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_sha") != decode_source_hash() or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- the workload
+
+def step_page_table(batch: int, seed: int = 1005):
+    """Contexts after this step's append: (indptr, indices, seq_lens, new_slots)."""
+    w, new_slots, _ = W.decode_step_workload(batch, seed=seed)
+    indptr, idx, lens = W.append_tokens(w, new_slots)
+    return w, indptr, idx, lens, new_slots
+
+
+def fill_pools(torch, M, pools, active_slots_d, layers, seed):
+    """Random non-NaN bytes everywhere; the active slots get N(0, 0.5) BF16
+    latents quantized by kv_store_fp8 with k_scale = absmax / 448."""
+    k_scales = []
+    n_active = active_slots_d.shape[0]
+    for l in range(layers):
+        g = torch.Generator(device=pools.device).manual_seed(seed * 1000 + l)
+        pool = pools[l]
+        pool.random_(0, 256, generator=g)
+        pool[(pool & 0x7F) == 0x7F] = 0x3C
+        lat = (torch.randn(n_active, 576, generator=g, device=pools.device) * 0.5).to(
+            torch.bfloat16)
+        ks = float(np.float32(lat.float().abs().max().item() / 448.0))
+        M.kv_store_fp8(lat[:, :512].contiguous(), lat[:, 512:].contiguous(), active_slots_d, ks,
+                       pool[:, :512], pool[:, 512:])
+        k_scales.append(ks)
+        del lat
+    return k_scales
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import mla_decode_attention_run_gb300 as M
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = init_dist(world, "nccl")
+    L, B, P = args.layers, args.batch, W.POOL_SLOTS
+    w, indptr, idx, lens, new_slots = step_page_table(B)
+    n_tok = int(lens.sum())
+
+    # ---- resident state: pools, per-layer q and new-token latents, outputs
+    pools = torch.empty(L, P, 576, dtype=torch.uint8, device=dev)
+    active_d = torch.from_numpy(w.kv_indices.astype(np.int64)).to(dev)
+    k_scales = fill_pools(torch, M, pools, active_d, L, seed=5)
+    gq = torch.Generator(device=dev).manual_seed(77)
+    q = torch.randn(L, B, HEADS, 576, generator=gq, device=dev).to(torch.bfloat16)
+    new_ckv = (torch.randn(L, B, 512, generator=gq, device=dev) * 0.5).to(torch.bfloat16)
+    new_kpe = (torch.randn(L, B, 64, generator=gq, device=dev) * 0.5).to(torch.bfloat16)
+    out = torch.empty(L, B, HEADS, 512, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(L, B, HEADS, dtype=torch.float32, device=dev)
+    indptr_d = torch.from_numpy(indptr).to(dev)
+    idx_d = torch.from_numpy(idx).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    slots_d = torch.from_numpy(new_slots).to(dev)
+    sm_scale = W.SOFTMAX_SCALE
+
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        plan = M.mla_decode_plan(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3, stream=stream)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    info = M.mla_decode_plan_info(plan)
+    launches_per_call = 1 + (1 if info["num_partials"] > 0 else 0)
+
+    def store(l, s):
+        M.kv_store_fp8(new_ckv[l], new_kpe[l], slots_d, k_scales[l], pools[l, :, :512],
+                       pools[l, :, 512:], stream=s)
+
+    def decode(l, s, pl=plan, ck=None, kp=None, ix=None, kscale=None):
+        M.mla_decode_run(pl, q[l], pools[l, :, :512] if ck is None else ck,
+                         pools[l, :, 512:] if kp is None else kp,
+                         P if ck is None else ck.shape[0], indptr_d,
+                         idx_d if ix is None else ix, lens_d,
+                         k_scales[l] if kscale is None else kscale, sm_scale, out[l], lse[l], ws,
+                         stream=s)
+
+    def capture(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            body(torch.cuda.current_stream())
+        return g
+
+    # one eager pass first (checks every call returns OK), then graphs
+    with torch.cuda.stream(stream):
+        for l in range(L):
+            store(l, stream)
+            decode(l, stream)
+    torch.cuda.synchronize()
+    flags = M.mla_get_last_error(stream)
+    if flags:
+        raise RuntimeError(f"device flags {flags:#x} after the eager pass")
+
+    g_step = capture(lambda s: [(store(l, s), decode(l, s)) for l in range(L)])
+    g_decode = capture(lambda s: [decode(l, s) for l in range(L)])
+
+    def plan_step():
+        M.mla_decode_plan(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3, stream=stream,
+                          plan=plan)
+
+    def timed(fn, steps):
+        barrier(dist)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        return e0.elapsed_time(e1)                     # ms
+
+    def full_step():
+        plan_step()
+        g_step.replay()
+
+    # ---- warm-up, then the K timed decode steps and K decode-only passes
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            full_step()
+            g_decode.replay()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            t_step = timed(full_step, args.steps)
+            t_dec = timed(g_decode.replay, args.steps)
+    clocks = clk.summary()
+    t_step = reduce_max(t_step, dist, dev)
+    t_dec = reduce_max(t_dec, dist, dev)
+    if M.mla_get_last_error(stream):
+        raise RuntimeError("device flags set during the timed region")
+
+    ms_per_step = t_step / args.steps
+    us_per_call = t_dec * 1e3 / (args.steps * L * world)     # whole job: all ranks' calls
+    call_bytes = A.decode_call_bytes(lens, HEADS, PAGE)
+    achieved = call_bytes / (t_dec * 1e-3 / (args.steps * L)) / 1e9
+    peak, peak_src = measured_peaks()
+    workload_name = f"decode_step_b{B}_h{HEADS}_l{L}"
+
+    result = {
+        "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16 mma / f32 accumulate (e4m3 cache)",
+        "data": "synthetic (seeded N(0,0.5) latents, N(0,1) q; no model weights)",
+        "config": {"workload": workload_name, "batch": B, "heads": HEADS, "layers": L,
+                   "page_size": PAGE, "pool_slots": P, "tokens_per_call": n_tok,
+                   "contexts": "uniform[1024,8192] + 1 appended", "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (78 pools, ~8.4 GB touched per step)",
+                   "graphs": "CUDA graph per step; plan rebuilt on the host each step"},
+        "decode_step_ms": round(ms_per_step, 4),
+        "tokens_per_s": round(B * world / (ms_per_step * 1e-3), 1),
+        # our kernels in the two timed regions: K steps of 78 x (store + decode
+        # [+ merge]) and K decode-only passes of 78 x (decode [+ merge])
+        "gpu_launches": int(args.steps * L * (1 + 2 * launches_per_call)),
+        "plan": info,
+        "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": committed_traffic(workload_name),
+                     "kernel": "mla_decode_run (decode kernel + split-KV merge)",
+                     "algorithmic_bytes_per_launch": call_bytes,
+                     "peak_source": f"{peak_src} HBM copy bandwidth"},
+    }
+
+    # ---- e2e through the public API from pinned host buffers
+    h_q = torch.empty_like(q, device="cpu").pin_memory()
+    h_q.copy_(q.cpu())
+    h_ckv = new_ckv.cpu().pin_memory()
+    h_kpe = new_kpe.cpu().pin_memory()
+    h_pt = [torch.from_numpy(a).pin_memory() for a in (indptr, idx, lens)]
+    h_slots = torch.from_numpy(new_slots).pin_memory()
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        new_ckv.copy_(h_ckv, non_blocking=True)
+        new_kpe.copy_(h_kpe, non_blocking=True)
+        for d, h in zip((indptr_d, idx_d, lens_d), h_pt):
+            d.copy_(h, non_blocking=True)
+        slots_d.copy_(h_slots, non_blocking=True)
+        full_step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        k_e2e = max(3, min(args.steps, 10))
+        t_e2e = reduce_max(timed(e2e_step, k_e2e), dist, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_ckv, h_kpe, *h_pt, h_slots))
+    d2h = h_out.numel() * h_out.element_size() + h_lse.numel() * h_lse.element_size()
+    result["e2e"] = {"value": round(t_e2e * 1e3 / (k_e2e * L * world), 3), "unit": "us/call",
+                     "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                     "per": "layer-call incl. store and host copies"}
+
+    # ---- the two baselines the pages describe, per decode step
+    if not args.no_baselines:
+        result["baselines"] = run_baselines(torch, M, args, stream, pools, q, out, lse, ws,
+                                            k_scales, store, indptr, idx, lens, timed, dist, dev)
+
+    # ---- CPU oracle baseline (rank 0, one GPU)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_from_device(pools[0], q[0], indptr, idx, lens,
+                                                          k_scales[0])
+    del g_step, g_decode
+    M.mla_decode_plan_destroy(plan)
+    return result
+
+
+def run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, store, indptr, idx,
+                  lens, timed, dist, dev):
+    L, B, P = args.layers, args.batch, W.POOL_SLOTS
+    n = idx.size
+    idx_d = torch.from_numpy(idx).to(dev)
+    indptr_d = torch.from_numpy(indptr).to(dev)
+    lens_d = torch.from_numpy(lens).to(dev)
+    seq_d = torch.arange(n, dtype=torch.int32, device=dev)
+    full = torch.empty(P, 576, dtype=torch.bfloat16, device=dev)
+    compact = torch.empty(n, 576, dtype=torch.bfloat16, device=dev)
+    with torch.cuda.stream(stream):
+        plan_bf16 = M.mla_decode_plan(indptr, lens, B, HEADS, PAGE, M.MLA_KV_BF16, stream=stream)
+    ws_b = torch.empty(max(plan_bf16.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+    sm = W.SOFTMAX_SCALE
+
+    def cast_layer(l, s):      # the pages' full-pool .to(bfloat16), then BF16 attention
+        full.copy_(pools[l].view(torch.float8_e4m3fn))
+        M.mla_decode_run(plan_bf16, q[l], full[:, :512], full[:, 512:], P, indptr_d, idx_d,
+                         lens_d, k_scales[l], sm, out[l], lse[l], ws_b, stream=s)
+
+    def gather_layer(l, s):    # gather-then-cast of the active slots, replan 0..n-1
+        M.kv_gather_cast(pools[l, :, :512], pools[l, :, 512:], idx_d, 1, 1.0, compact[:, :512],
+                         compact[:, 512:], stream=s)
+        M.mla_decode_run(plan_bf16, q[l], compact[:, :512], compact[:, 512:], n, indptr_d, seq_d,
+                         lens_d, k_scales[l], sm, out[l], lse[l], ws_b, stream=s)
+
+    res = {}
+    for name, layer_fn in (("full_pool_cast_then_bf16_decode", cast_layer),
+                           ("gather_then_cast_then_bf16_decode", gather_layer)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            s = torch.cuda.current_stream()
+            for l in range(L):
+                store(l, s)
+                layer_fn(l, s)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            k = max(3, min(args.steps, 5))
+            t = reduce_max(timed(g.replay, k), dist, dev)
+        res[name] = {"decode_step_ms": round(t / k, 3)}
+        del g
+    cast_bytes = A.full_pool_cast_bytes(P) * L
+    gather_bytes = A.gather_cast_bytes(n, n) * L
+    res["full_pool_cast_then_bf16_decode"]["cast_bytes_per_step"] = cast_bytes
+    res["gather_then_cast_then_bf16_decode"]["cast_bytes_per_step"] = gather_bytes
+    M.mla_decode_plan_destroy(plan_bf16)
+    return res
+
+
+def oracle_call(pool_np, q_bits, indptr, idx, lens, k_scale, nthreads=0):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.decode_fp8(q_bits, pool_np[:, :512], pool_np[:, 512:], indptr, idx, lens, PAGE,
+                      k_scale, W.SOFTMAX_SCALE, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_from_device(pool_d, q_d, indptr, idx, lens, k_scale):
+    import oracle
+    import torch
+    pool_np = pool_d.cpu().numpy()
+    q_bits = q_d.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    threads = oracle.max_threads()
+    dt = oracle_call(pool_np, q_bits, indptr, idx, lens, k_scale)
+    return {"value": round(dt * 1e6, 1), "unit": "us/call", "cores": threads, "kind": "oracle",
+            "sample": "one layer's full decode call (batch 40, 16 heads, all contexts), "
+                      "C fp64 oracle with OpenMP over (request, head)"}
+
+
+def run_reference(args, rank, world, local):
+    """The reference arm: the CPU oracle, as it stands, on the same decode
+    call (one layer of the batch-40 step), each step one full call."""
+    if rank != 0:
+        return None
+    import oracle
+    w, indptr, idx, lens, new_slots = step_page_table(args.batch)
+    wl = W.make_workload("concurrency", batch=args.batch, seed=1005)   # same page table
+    pool = W.random_fill_bytes(np.random.default_rng(5), (W.POOL_SLOTS, 576))
+    oracle.kv_store_fp8(wl.latent_bf16[:, :512], wl.latent_bf16[:, 512:], wl.latent_slots,
+                        wl.k_scale, pool[:, :512], pool[:, 512:])
+    new = W.make_workload("concurrency", batch=args.batch, lens=[1] * args.batch, seed=99)
+    oracle.kv_store_fp8(new.latent_bf16[:, :512], new.latent_bf16[:, 512:], new_slots,
+                        wl.k_scale, pool[:, :512], pool[:, 512:])
+    q_bits = wl.q_bf16
+    for _ in range(args.warmup):
+        oracle_call(pool, q_bits, indptr, idx, lens, wl.k_scale)
+    times = [oracle_call(pool, q_bits, indptr, idx, lens, wl.k_scale) for _ in range(args.steps)]
+    us = float(np.mean(times)) * 1e6
+    cores = oracle.max_threads()
+    sample = ("one layer's full decode call per step (batch 40, 16 heads, contexts "
+              "uniform[1024,8192]+1), C fp64 oracle, OpenMP over (request, head)")
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/call",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"decode_step_b{args.batch}_h{HEADS}_l{args.layers}",
+                       "batch": args.batch, "heads": HEADS, "page_size": PAGE,
+                       "tokens_per_call": int(lens.sum()), "parallelism": "replicas"},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=40)
+    ap.add_argument("--layers", type=int, default=W.NUM_LAYERS)
+    ap.add_argument("--no-baselines", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world, local)
+    else:
+        res = run_ours(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

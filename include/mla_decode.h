@@ -1,0 +1,224 @@
+/*
+ * mla_decode.h -- C ABI of libmla_decode.so: paged MLA decode attention that
+ * reads an FP8 E4M3 KV cache directly, plus its two companion kernels
+ * (quantize-on-store and active-slot gather-then-cast).  One GPU (sm_103a).
+ *
+ * Sources (web pages, by title and section):
+ *  [P1] "When a Faster Kernel Doesn't Speed Up Serving: Profiling FP8 KV
+ *       Cache on AMD Instinct MI308X": "Setup" (--kv-cache-dtype fp8_e4m3,
+ *       a 16-head q_len-1 MLA decode kernel), "Step 3: Source Validation"
+ *       (CastFromFP8 / CastToFP8: the FP8<->BF16 casts on the cache read and
+ *       write paths).
+ *  [P2] "The KV Cache Cast Bottleneck: A Surgical Fix for 69% Decode
+ *       Overhead": "The Context" (cache rows [495552, 1, 576] of
+ *       Float8_e4m3fn; 576 = kv_lora_rank 512 + qk_rope_head_dim 64),
+ *       "The Message" (plan() takes separate query and KV data types; the
+ *       attention kernel reads FP8 rows and computes in higher precision).
+ *  [P3] "The Gather-Then-Cast Pivot": "The Subject Message" (run() reads
+ *       page-indexed ckv/kpe buffers; kv_indices from plan() say which slots),
+ *       "The Reasoning Process" (gather the active FP8 rows into a compact
+ *       buffer, cast it, replan with sequential indices).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named *_host are host memory; every other data pointer is
+ *    device memory owned by the caller.  The library owns only plan handles.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every call that launches work is asynchronous on it.
+ *  - Host-detectable errors (NULL pointers, bad sizes, misalignment, an
+ *    inconsistent page table, a small workspace) return a status before any
+ *    launch and leave every output untouched.
+ *  - Device-detected problems (a slot or page index outside the pool) never
+ *    trap: the offending row is skipped (store / gather: its destination is
+ *    left unwritten; decode: the token is excluded from the softmax) and a
+ *    bit is OR-ed into a device flag word that mla_get_last_error() reads.
+ *  - FP8 means OCP E4M3: bias 7, largest finite 448, 0x7F / 0xFF are NaN, no
+ *    infinities.  BF16 tensors hold raw bfloat16 values.
+ *  - Pool layout: row `slot` of the c_kv pool starts at
+ *    ckv_pool + slot * ckv_row_stride_bytes and holds 512 channels; row
+ *    `slot` of the k_pe pool starts at kpe_pool + slot * kpe_row_stride_bytes
+ *    and holds 64 channels.  The pages' combined [slots, 576] layout is
+ *    kpe_pool = ckv_pool + 512 elements with both strides = one 576-row.
+ *    Pool base pointers and row strides must be multiples of 16 bytes.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,  /* NULL pointer, bad size, bad page table     */
+    MLA_ERR_UNSUPPORTED = 2,  /* head count / alignment the kernels lack    */
+    MLA_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than planned     */
+    MLA_ERR_INDEX_OOB = 4,    /* reported by mla_get_last_error()           */
+    MLA_ERR_CUDA = 5          /* a CUDA runtime call failed                 */
+} mla_status_t;
+
+typedef enum {
+    MLA_KV_FP8_E4M3 = 0,      /* the product path: pools hold E4M3 bytes    */
+    MLA_KV_BF16 = 1           /* pools hold BF16 (cast-then-attend baselines) */
+} mla_kv_dtype_t;
+
+/* Bits of the device flag word read by mla_get_last_error(). */
+#define MLA_FLAG_INDEX_OOB      0x1u  /* a slot / page index was outside the pool */
+#define MLA_FLAG_PLAN_MISMATCH  0x2u  /* device seq_lens disagree with the plan  */
+#define MLA_FLAG_WAIT_TIMEOUT   0x4u  /* a bounded in-kernel wait gave up        */
+
+typedef struct mla_plan* mla_plan_t;
+
+#define MLA_D_CKV 512   /* kv_lora_rank   ([P2] "The Context") */
+#define MLA_D_KPE 64    /* qk_rope_head_dim ([P2] "The Context") */
+#define MLA_D_QK  576   /* score width = 512 + 64 */
+
+/*
+ * mla_decode_plan -- the plan() half of the plan/run split ([P2] "The
+ * Message"; [P3] "The Subject Message").  Runs on the host once per decode
+ * step, shared by all layers of that step.
+ *
+ *  plan             in/out.  If *plan is NULL a new plan is created;
+ *                   otherwise that plan is rebuilt in place (its device and
+ *                   pinned buffers are reused when large enough).
+ *  kv_indptr_host   int32 [batch+1]: request b owns page-table entries
+ *                   kv_indices[kv_indptr[b] .. kv_indptr[b+1]).  Must be
+ *                   non-decreasing, kv_indptr[0] >= 0, and each request must
+ *                   own exactly ceil(seq_lens[b] / page_size) pages.
+ *  seq_lens_host    int32 [batch]: context length of each request (>= 0).
+ *  num_heads        query heads H: 1..16, or a multiple of 16 up to 128.
+ *  page_size        tokens per page (>= 1).  Token t of request b is slot
+ *                   kv_indices[kv_indptr[b] + t / page_size] * page_size
+ *                   + t % page_size.
+ *  kv_dtype         element type of the pools run() will read.
+ *  workspace_bytes  out: device scratch run() needs (split-KV partials).
+ *  stream           the plan's device metadata is uploaded on this stream
+ *                   (stream-ordered before later runs on it).
+ * Errors: MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED before any allocation;
+ * MLA_ERR_CUDA if an allocation or copy fails (the plan stays valid if it
+ * existed).  The plan must be rebuilt whenever kv_indptr or seq_lens change.
+ */
+mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indptr_host,
+                             const int32_t* seq_lens_host, int32_t batch,
+                             int32_t num_heads, int32_t page_size,
+                             mla_kv_dtype_t kv_dtype, size_t* workspace_bytes,
+                             void* stream);
+
+/*
+ * mla_decode_run -- the run() half: decode attention for every request of
+ * the plan, reading the cache rows in place (no BF16 copy of the cache is
+ * made).  Per request b and head h, with k_t = value(row_t) * k_scale over
+ * all 576 channels (c_kv then k_pe) and v_t = the 512 c_kv channels:
+ *     s_t = softmax_scale * sum_d q[b][h][d] * k_t[d]
+ *     out[b][h] = sum_t softmax(s)_t * v_t        (BF16)
+ *     lse[b][h] = ln sum_t exp(s_t)               (fp32, natural log)
+ * A request with seq_len 0 gets out = 0 and lse = -inf.
+ *
+ *  q                BF16, element (b, h, d) at q + b*q_stride_b + h*q_stride_h
+ *                   + d (strides in elements; d < 576 contiguous).
+ *  ckv_pool, ...    see the pool layout above; E4M3 bytes for
+ *                   MLA_KV_FP8_E4M3 plans, BF16 for MLA_KV_BF16 plans.
+ *  num_pool_slots   rows in each pool; indices reaching past it are skipped.
+ *  kv_indptr_dev, kv_indices_dev, seq_lens_dev
+ *                   device copies of the page table given to the plan
+ *                   (kv_indptr / seq_lens must equal the plan's host arrays).
+ *  k_scale          per-tensor dequantization scale (use 1 for BF16 pools
+ *                   that already hold real values).
+ *  out              BF16 [batch][H][512], contiguous.
+ *  lse              fp32 [batch][H], contiguous.
+ *  workspace        device scratch of at least the planned workspace_bytes,
+ *                   256-byte aligned; its contents are not preserved.
+ * No host synchronisation, allocation or host<->device copy happens here.
+ * Errors: MLA_ERR_INVALID_ARG (NULL / misaligned / plan mismatch),
+ * MLA_ERR_WORKSPACE, MLA_ERR_CUDA (launch failure).
+ */
+mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q_stride_b,
+                            int64_t q_stride_h, const void* ckv_pool,
+                            int64_t ckv_row_stride_bytes, const void* kpe_pool,
+                            int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
+                            const int32_t* kv_indptr_dev,
+                            const int32_t* kv_indices_dev,
+                            const int32_t* seq_lens_dev, float k_scale,
+                            float softmax_scale, void* out, float* lse,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* Releases a plan and its device / pinned buffers (after the caller has
+ * synchronised any stream still using it).  NULL is accepted. */
+mla_status_t mla_decode_plan_destroy(mla_plan_t plan);
+
+/* Plan summary: CTAs launched, (cta, request, token range) segments, split
+ * partials written to the workspace, and the workspace size.  Host only. */
+mla_status_t mla_decode_plan_info(mla_plan_t plan, int32_t* num_ctas,
+                                  int32_t* num_segments, int32_t* num_partials,
+                                  size_t* workspace_bytes);
+
+/*
+ * mla_decode_schedule -- host only, no GPU needed: the split-KV schedule a
+ * plan with these arguments would use on a GPU with `num_sms` SMs.  Writes
+ * up to `capacity` segments as int32 quintuples
+ *     (cta, request, token_begin, token_end, partial_index or -1)
+ * into segments_out (may be NULL), in launch order.  Validates exactly like
+ * mla_decode_plan.
+ */
+mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
+                                 const int32_t* seq_lens_host, int32_t batch,
+                                 int32_t num_heads, int32_t page_size,
+                                 mla_kv_dtype_t kv_dtype, int32_t num_sms,
+                                 int32_t* segments_out, int32_t capacity,
+                                 int32_t* num_segments, int32_t* num_partials,
+                                 int32_t* num_ctas, size_t* workspace_bytes);
+
+/*
+ * kv_store_fp8 -- quantize-on-store scatter ([P1] "Step 3", CastToFP8 in
+ * set_kv_buffer), fused into one pass: for each new token i,
+ *     ckv_pool[slots[i]][d] = E4M3(float(ckv_new[i][d]) / k_scale), d < 512
+ *     kpe_pool[slots[i]][d] = E4M3(float(kpe_new[i][d]) / k_scale), d < 64
+ * with one IEEE fp32 division, round to nearest (ties to even), saturation
+ * of |x| > 448 (and +-inf) to +-448, NaN -> 0x7F, sign kept.
+ *  ckv_new  BF16 [n][512] contiguous;  kpe_new  BF16 [n][64] contiguous.
+ *  slots    int64 [n], device.  Duplicate slots give an unspecified row.
+ * n = 0 is a no-op.  Errors: MLA_ERR_INVALID_ARG, MLA_ERR_CUDA.
+ */
+mla_status_t kv_store_fp8(const void* ckv_new, const void* kpe_new,
+                          const int64_t* slots, int64_t n, float k_scale,
+                          void* ckv_pool, int64_t ckv_row_stride_bytes,
+                          void* kpe_pool, int64_t kpe_row_stride_bytes,
+                          int64_t num_pool_slots, void* stream);
+
+/*
+ * kv_gather_cast -- gather-then-cast of the active pages ([P3] "The
+ * Reasoning Process"): row j*page_size + r of the outputs is pool slot
+ * kv_indices[j]*page_size + r, converted as
+ *     BF16_rne(float(value(byte)) * k_scale)
+ * (one fp32 multiply; with k_scale = 1 this is exactly the pages' unscaled
+ * .to(bfloat16)).  A caller then replans with indices 0..n_pages-1 and runs a
+ * MLA_KV_BF16 decode on the compact buffers.
+ *  kv_indices  int32 [n_pages], device.
+ *  ckv_out     BF16 [n_pages*page_size][512];  kpe_out  BF16 [..][64].
+ * n_pages = 0 is a no-op.  Errors: MLA_ERR_INVALID_ARG, MLA_ERR_CUDA.
+ */
+mla_status_t kv_gather_cast(const void* ckv_pool, int64_t ckv_row_stride_bytes,
+                            const void* kpe_pool, int64_t kpe_row_stride_bytes,
+                            int64_t num_pool_slots, const int32_t* kv_indices,
+                            int64_t n_pages, int32_t page_size, float k_scale,
+                            void* ckv_out, void* kpe_out, void* stream);
+
+/*
+ * mla_get_last_error -- synchronises `stream`, then reads and clears the
+ * current device's flag word (MLA_FLAG_* bits, OR-ed by every kernel since
+ * the last call).  Returns MLA_ERR_INDEX_OOB if any flag was set,
+ * MLA_ERR_CUDA if the synchronisation failed, else MLA_OK.
+ */
+mla_status_t mla_get_last_error(void* stream, uint32_t* device_flags_out);
+
+/* Static description of a status code. */
+const char* mla_status_string(mla_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

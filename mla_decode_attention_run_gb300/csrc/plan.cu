@@ -1,0 +1,266 @@
+// mla_decode_plan / mla_decode_schedule: the plan() half of the plan/run
+// split ("The KV Cache Cast Bottleneck", section "The Message": plan() is
+// told the query and KV data types; "The Gather-Then-Cast Pivot", section
+// "The Subject Message": plan() fixes which pool slots run() reads).
+//
+// The schedule balances work by tokens, not by requests: with contexts drawn
+// from [1024, 8192] a per-request split leaves SMs idle, so the tile list of
+// all requests is cut into equal contiguous ranges (one per CTA).
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace mla {
+namespace {
+
+bool heads_supported(int32_t h) { return (h >= 1 && h <= 16) || (h > 16 && h <= 128 && h % 16 == 0); }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Resident decode CTAs per SM for a plan (the kernel's shared-memory budget
+// allows one).
+int ctas_per_sm(mla_kv_dtype_t) { return 1; }
+
+// A CTA gets at least this many tiles when there is enough work.
+constexpr int64_t kMinTilesPerCta = 2;
+
+}  // namespace
+
+mla_status_t validate_plan_inputs(const int32_t* indptr, const int32_t* seq, int32_t B,
+                                  int32_t H, int32_t ps, mla_kv_dtype_t dtype) {
+    if (!indptr || !seq) return MLA_ERR_INVALID_ARG;
+    if (B < 1 || B > (1 << 24) || ps < 1 || ps > (1 << 20)) return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_KV_FP8_E4M3 && dtype != MLA_KV_BF16) return MLA_ERR_INVALID_ARG;
+    if (!heads_supported(H)) return MLA_ERR_UNSUPPORTED;
+    if (indptr[0] < 0) return MLA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < B; ++b) {
+        if (seq[b] < 0) return MLA_ERR_INVALID_ARG;
+        const int64_t pages = static_cast<int64_t>(indptr[b + 1]) - indptr[b];
+        if (pages != (static_cast<int64_t>(seq[b]) + ps - 1) / ps) return MLA_ERR_INVALID_ARG;
+    }
+    return MLA_OK;
+}
+
+mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B, int32_t H,
+                            int32_t ps, mla_kv_dtype_t dtype, int32_t num_sms, Schedule& s) {
+    const mla_status_t st = validate_plan_inputs(indptr, seq, B, H, ps, dtype);
+    if (st != MLA_OK) return st;
+    if (num_sms < 1) return MLA_ERR_INVALID_ARG;
+    int64_t n_tokens = 0, n_tiles = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        n_tokens += seq[b];
+        n_tiles += (seq[b] + kTileTokens - 1) / kTileTokens;
+    }
+
+    s = Schedule();
+    s.batch = B;
+    s.heads = H;
+    s.page_size = ps;
+    s.kv_dtype = dtype;
+    s.n_tokens = n_tokens;
+    s.head_groups = (H + kHeadsPerCta - 1) / kHeadsPerCta;
+
+    int64_t ctas = static_cast<int64_t>(num_sms) * ctas_per_sm(dtype) / s.head_groups;
+    if (ctas < 1) ctas = 1;
+    const int64_t by_work = (n_tiles + kMinTilesPerCta - 1) / kMinTilesPerCta;
+    if (ctas > by_work) ctas = by_work;
+    s.num_ctas = static_cast<int32_t>(ctas);
+
+    // request tile offsets in the concatenated tile list
+    std::vector<int64_t> first_tile(B + 1, 0);
+    for (int32_t b = 0; b < B; ++b)
+        first_tile[b + 1] = first_tile[b] + (seq[b] + kTileTokens - 1) / kTileTokens;
+
+    std::vector<int32_t> segs_per_req(B, 0);
+    s.cta_ptr.assign(s.num_ctas + 1, 0);
+    int32_t b = 0;
+    for (int32_t c = 0; c < s.num_ctas; ++c) {
+        s.cta_ptr[c] = static_cast<int32_t>(s.segs.size() / 4);
+        const int64_t lo = n_tiles * c / s.num_ctas, hi = n_tiles * (c + 1) / s.num_ctas;
+        int64_t pos = lo;
+        while (pos < hi) {
+            while (first_tile[b + 1] <= pos) ++b;       // skips empty requests too
+            const int64_t end = hi < first_tile[b + 1] ? hi : first_tile[b + 1];
+            const int64_t t0 = (pos - first_tile[b]) * kTileTokens;
+            int64_t t1 = (end - first_tile[b]) * kTileTokens;
+            if (t1 > seq[b]) t1 = seq[b];
+            s.segs.insert(s.segs.end(), {b, static_cast<int32_t>(t0), static_cast<int32_t>(t1), -1});
+            ++segs_per_req[b];
+            pos = end;
+        }
+    }
+    s.cta_ptr[s.num_ctas] = static_cast<int32_t>(s.segs.size() / 4);
+
+    // partial slots: consecutive per request, in launch order
+    std::vector<int32_t> first_partial(B, -1);
+    for (int32_t i = 0; i < s.n_segs(); ++i) {
+        const int32_t r = s.segs[4 * i];
+        if (segs_per_req[r] > 1) {
+            if (first_partial[r] < 0) first_partial[r] = s.n_partials;
+            s.segs[4 * i + 3] = s.n_partials++;
+        }
+    }
+    for (int32_t r = 0; r < B; ++r) {
+        if (segs_per_req[r] > 1) s.merge.insert(s.merge.end(), {r, first_partial[r], segs_per_req[r]});
+        else if (seq[r] == 0) s.merge.insert(s.merge.end(), {r, 0, 0});
+    }
+
+    const size_t o_bytes = static_cast<size_t>(s.n_partials) * H * kDCkv * sizeof(float);
+    s.partial_lse_offset = align256(o_bytes);
+    s.workspace_bytes =
+        s.n_partials ? align256(s.partial_lse_offset + static_cast<size_t>(s.n_partials) * H * 4) : 0;
+    return MLA_OK;
+}
+
+}  // namespace mla
+
+using mla::Schedule;
+
+extern "C" mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
+                                            const int32_t* seq_lens_host, int32_t batch,
+                                            int32_t num_heads, int32_t page_size,
+                                            mla_kv_dtype_t kv_dtype, int32_t num_sms,
+                                            int32_t* segments_out, int32_t capacity,
+                                            int32_t* num_segments, int32_t* num_partials,
+                                            int32_t* num_ctas, size_t* workspace_bytes) {
+    Schedule s;
+    const mla_status_t st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads,
+                                                page_size, kv_dtype, num_sms, s);
+    if (st != MLA_OK) return st;
+    if (segments_out) {
+        int32_t k = 0;
+        for (int32_t c = 0; c < s.num_ctas; ++c) {
+            for (int32_t i = s.cta_ptr[c]; i < s.cta_ptr[c + 1] && k < capacity; ++i, ++k) {
+                int32_t* d = segments_out + 5 * k;
+                d[0] = c;
+                std::memcpy(d + 1, &s.segs[4 * i], 4 * sizeof(int32_t));
+            }
+        }
+    }
+    if (num_segments) *num_segments = s.n_segs();
+    if (num_partials) *num_partials = s.n_partials;
+    if (num_ctas) *num_ctas = s.num_ctas;
+    if (workspace_bytes) *workspace_bytes = s.workspace_bytes;
+    return MLA_OK;
+}
+
+namespace {
+
+void release_buffers(mla_plan* p) {
+    if (p->dev_meta) cudaFree(p->dev_meta);
+    if (p->pinned) cudaFreeHost(p->pinned);
+    if (p->upload_done) cudaEventDestroy(p->upload_done);
+    p->dev_meta = nullptr;
+    p->pinned = nullptr;
+    p->upload_done = nullptr;
+    p->dev_meta_cap = p->pinned_cap = 0;
+}
+
+}  // namespace
+
+extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indptr_host,
+                                        const int32_t* seq_lens_host, int32_t batch,
+                                        int32_t num_heads, int32_t page_size,
+                                        mla_kv_dtype_t kv_dtype, size_t* workspace_bytes,
+                                        void* stream) {
+    if (!plan || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+    mla_status_t st = mla::validate_plan_inputs(kv_indptr_host, seq_lens_host, batch, num_heads,
+                                                page_size, kv_dtype);
+    if (st != MLA_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+    const int sms = mla::device_sm_count();
+    if (sms <= 0) return MLA_ERR_CUDA;
+    Schedule s;
+    st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads, page_size,
+                             kv_dtype, sms, s);
+    if (st != MLA_OK) return st;
+
+    mla_plan* p = *plan;
+    const bool fresh = (p == nullptr);
+    if (fresh) {
+        p = new (std::nothrow) mla_plan();
+        if (!p) return MLA_ERR_CUDA;
+    } else if (p->device != dev) {
+        return MLA_ERR_INVALID_ARG;       // a plan belongs to one device
+    }
+    p->device = dev;
+    const size_t need = static_cast<size_t>(s.num_ctas + 1) + s.segs.size() + s.merge.size();
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+    if (!p->upload_done &&
+        cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming) != cudaSuccess) {
+        if (fresh) { release_buffers(p); delete p; }
+        return MLA_ERR_CUDA;
+    }
+    // the previous upload must be finished before the staging buffer is reused
+    if (cudaEventSynchronize(p->upload_done) != cudaSuccess) {
+        if (fresh) { release_buffers(p); delete p; }
+        return MLA_ERR_CUDA;
+    }
+    if (p->pinned_cap < need) {
+        if (p->pinned) cudaFreeHost(p->pinned);
+        p->pinned = nullptr;
+        p->pinned_cap = 0;
+        size_t cap = need < 1024 ? 1024 : need * 2;
+        if (cudaHostAlloc(reinterpret_cast<void**>(&p->pinned), cap * sizeof(int32_t),
+                          cudaHostAllocDefault) != cudaSuccess) {
+            if (fresh) { release_buffers(p); delete p; }
+            return MLA_ERR_CUDA;
+        }
+        p->pinned_cap = cap;
+    }
+    if (p->dev_meta_cap < need) {
+        // growing: earlier runs may still read the old buffer; cudaFree waits
+        // for the device before releasing it
+        if (p->dev_meta) cudaFree(p->dev_meta);
+        p->dev_meta = nullptr;
+        p->dev_meta_cap = 0;
+        size_t cap = need < 1024 ? 1024 : need * 2;
+        if (cudaMalloc(reinterpret_cast<void**>(&p->dev_meta), cap * sizeof(int32_t)) !=
+            cudaSuccess) {
+            if (fresh) { release_buffers(p); delete p; }
+            return MLA_ERR_CUDA;
+        }
+        p->dev_meta_cap = cap;
+    }
+    p->off_cta = 0;
+    p->off_segs = s.num_ctas + 1;
+    p->off_merge = p->off_segs + s.segs.size();
+    std::memcpy(p->pinned + p->off_cta, s.cta_ptr.data(), (s.num_ctas + 1) * sizeof(int32_t));
+    if (!s.segs.empty())
+        std::memcpy(p->pinned + p->off_segs, s.segs.data(), s.segs.size() * sizeof(int32_t));
+    if (!s.merge.empty())
+        std::memcpy(p->pinned + p->off_merge, s.merge.data(), s.merge.size() * sizeof(int32_t));
+    if (cudaMemcpyAsync(p->dev_meta, p->pinned, need * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        cs) != cudaSuccess ||
+        cudaEventRecord(p->upload_done, cs) != cudaSuccess) {
+        if (fresh) { release_buffers(p); delete p; }
+        return MLA_ERR_CUDA;
+    }
+    p->sched = std::move(s);
+    *workspace_bytes = p->sched.workspace_bytes;
+    *plan = p;
+    return MLA_OK;
+}
+
+extern "C" mla_status_t mla_decode_plan_destroy(mla_plan_t plan) {
+    if (!plan) return MLA_OK;
+    if (plan->upload_done) cudaEventSynchronize(plan->upload_done);
+    release_buffers(plan);
+    delete plan;
+    return MLA_OK;
+}
+
+extern "C" mla_status_t mla_decode_plan_info(mla_plan_t plan, int32_t* num_ctas,
+                                             int32_t* num_segments, int32_t* num_partials,
+                                             size_t* workspace_bytes) {
+    if (!plan) return MLA_ERR_INVALID_ARG;
+    if (num_ctas) *num_ctas = plan->sched.num_ctas;
+    if (num_segments) *num_segments = plan->sched.n_segs();
+    if (num_partials) *num_partials = plan->sched.n_partials;
+    if (workspace_bytes) *workspace_bytes = plan->sched.workspace_bytes;
+    return MLA_OK;
+}

@@ -1,0 +1,59 @@
+// Host planner shared by plan.cu (construction) and decode.cu (launch).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+// Tokens per KV tile of the decode kernel, and heads per CTA.
+constexpr int kTileTokens = 64;
+constexpr int kHeadsPerCta = 16;
+
+// The split-KV schedule.  The concatenation of all requests' tiles is cut
+// into `num_ctas` contiguous, equal-sized (+-1 tile) ranges; each range is a
+// CTA (per head group), and each piece of a range that lies in one request
+// is a segment.  A request covered by one segment is written directly; the
+// segments of a request covered by several write fp32 partials (normalised
+// o and lse) that the merge kernel combines.
+struct Schedule {
+    int32_t batch = 0, heads = 0, page_size = 0;
+    mla_kv_dtype_t kv_dtype = MLA_KV_FP8_E4M3;
+    int32_t head_groups = 0;
+    int32_t num_ctas = 0;            // token ranges; grid = num_ctas * head_groups
+    std::vector<int32_t> cta_ptr;    // [num_ctas + 1] -> segment index
+    std::vector<int32_t> segs;       // 4 per segment: request, t0, t1, partial (-1 = final)
+    std::vector<int32_t> merge;      // 3 per entry: request, first partial, n partials
+    int32_t n_partials = 0;
+    int64_t n_tokens = 0;
+    size_t partial_lse_offset = 0;   // bytes into the workspace
+    size_t workspace_bytes = 0;
+
+    int32_t n_segs() const { return static_cast<int32_t>(segs.size() / 4); }
+    int32_t n_merge() const { return static_cast<int32_t>(merge.size() / 3); }
+};
+
+mla_status_t validate_plan_inputs(const int32_t* kv_indptr, const int32_t* seq_lens,
+                                  int32_t batch, int32_t heads, int32_t page_size,
+                                  mla_kv_dtype_t kv_dtype);
+
+mla_status_t build_schedule(const int32_t* kv_indptr, const int32_t* seq_lens, int32_t batch,
+                            int32_t heads, int32_t page_size, mla_kv_dtype_t kv_dtype,
+                            int32_t num_sms, Schedule& out);
+
+}  // namespace mla
+
+struct mla_plan {
+    mla::Schedule sched;
+    int device = -1;
+    int32_t* dev_meta = nullptr;      // cta_ptr | segs | merge (int32)
+    size_t dev_meta_cap = 0;          // elements
+    int32_t* pinned = nullptr;        // staging for the upload
+    size_t pinned_cap = 0;
+    cudaEvent_t upload_done = nullptr;
+    size_t off_cta = 0, off_segs = 0, off_merge = 0;   // element offsets in dev_meta
+};

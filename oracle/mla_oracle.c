@@ -142,6 +142,8 @@ int64_t oracle_kv_store_fp8(const uint16_t* ckv_new, const uint16_t* kpe_new,
                             uint8_t* kpe_pool, int64_t kpe_stride,
                             int64_t num_slots) {
     int64_t bad = 0;
+    /* tokens are independent: one per iteration */
+#pragma omp parallel for schedule(static) reduction(+ : bad)
     for (int64_t i = 0; i < n; ++i) {
         int64_t s = slots[i];
         if (s < 0 || s >= num_slots) { ++bad; continue; }

@@ -93,9 +93,12 @@ def random_fill_bytes(gen: np.random.Generator, shape) -> np.ndarray:
 def make_workload(name: str, *, batch: int | None = None, heads: int | None = None,
                   lens=None, page_size: int | None = None, num_slots: int | None = None,
                   seed: int | None = None, std: float | None = None,
-                  k_scale: float | None = None) -> Workload:
+                  k_scale: float | None = None, latent_requests=None) -> Workload:
     """Build one seeded workload.  Keyword overrides give smaller variants of
-    a named config (same recipe, other sizes)."""
+    a named config (same recipe, other sizes).  latent_requests, if given,
+    limits the drawn latents to those requests' slots (the other active
+    slots are left to the caller, e.g. random bytes): the H=128 long-context
+    pool holds 2.4 G latents, and a parity check needs only a sample."""
     cfg = dict(CONFIGS[name])
     B = batch if batch is not None else cfg["batch"]
     H = heads if heads is not None else cfg["heads"]
@@ -126,7 +129,8 @@ def make_workload(name: str, *, batch: int | None = None, heads: int | None = No
     # slots actually holding tokens (every row of every listed page that a
     # token of the request covers)
     slot_list = []
-    for b in range(B):
+    chosen = range(B) if latent_requests is None else sorted(set(latent_requests))
+    for b in chosen:
         pg = kv_indices[kv_indptr[b]:kv_indptr[b + 1]].astype(np.int64)
         t = np.arange(seq[b], dtype=np.int64)
         slot_list.append(pg[t // ps] * ps + t % ps)
@@ -135,7 +139,7 @@ def make_workload(name: str, *, batch: int | None = None, heads: int | None = No
     lat = torch.randn((slots.shape[0], D_ALL), generator=g, dtype=torch.float32) * sd
     lat_bf16 = lat.to(torch.bfloat16)
     if k_scale is None:
-        if cfg["number"] == 1 and std is None:
+        if (cfg["number"] == 1 and std is None) or slots.shape[0] == 0:   # no latents drawn
             k_scale = 1.0
         else:
             k_scale = float(lat_bf16.float().abs().max().item()) / 448.0
@@ -147,17 +151,18 @@ def make_workload(name: str, *, batch: int | None = None, heads: int | None = No
                     k_scale=float(k_scale), seed=seed)
 
 
-def decode_step_workload(batch: int, layers: int = NUM_LAYERS, seed: int = 1005):
+def decode_step_workload(batch: int, layers: int = NUM_LAYERS, seed: int = 1005,
+                         with_latents: bool = False):
     """The full decode step: per layer the same page table, a new token per
     request appended into a random free slot (so each context grows by one),
     and per-layer latents / queries.  Returns the base workload (contexts
-    before the append), the new slots [B] and the new lengths."""
+    before the append), the new slots [B] and the number of layers."""
     lens = [4096] if batch == 1 else "uniform"
     w = make_workload("single" if batch == 1 else "concurrency", batch=batch, lens=lens,
-                      seed=seed)
+                      seed=seed, latent_requests=None if with_latents else [])
     g = np.random.default_rng(seed)
     used = np.zeros(w.num_slots, bool)
-    used[w.latent_slots] = True
+    used[w.kv_indices] = True                      # page size 1: pages are slots
     free = np.flatnonzero(~used)
     new_slots = g.choice(free, size=batch, replace=False).astype(np.int64)
     return w, new_slots, layers
