@@ -48,7 +48,8 @@ struct Smem {
     static constexpr size_t kRed = kP + size_t(kHeadsPerCta) * kPRow * 2;
     static constexpr size_t kL = kRed + size_t(kWarps) * kHeadsPerCta * 4;
     static constexpr size_t kCoef = kL + size_t(kWarps) * kHeadsPerCta * 4;
-    static constexpr size_t kBytes = kCoef + size_t(kHeadsPerCta) * 4;
+    static constexpr size_t kMask = kCoef + size_t(kHeadsPerCta) * 4;   // 4 tiles x 64 rows
+    static constexpr size_t kBytes = kMask + size_t(4) * kT;
 };
 
 struct DecodeParams {
@@ -91,11 +92,13 @@ __device__ __forceinline__ int64_t fetch_slot(const DecodeParams& p, const int32
     return slot;
 }
 
-// Gather the 16 rows of this warp (rows warp + 4k) into a raw stage.
+// Gather the 16 rows of this warp (rows warp + 4k) into a raw stage and
+// record which rows hold a real token (mask ring slot for this tile).
 template <bool kFp8>
 __device__ __forceinline__ void issue_rows(const DecodeParams& p, uint8_t* stage, int64_t slot_reg,
-                                           int warp, int lane) {
+                                           uint8_t* mask, int warp, int lane) {
     using S = Smem<kFp8>;
+    if (lane < 16) mask[warp + 4 * lane] = slot_reg >= 0 ? 1 : 0;
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
         const int64_t s = __shfl_sync(0xffffffffu, slot_reg, k);
@@ -127,6 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
     float* sRed = reinterpret_cast<float*>(smem + S::kRed);
     float* sL = reinterpret_cast<float*>(smem + S::kL);
     float* sCoef = reinterpret_cast<float*>(smem + S::kCoef);
+    uint8_t* sMask = smem + S::kMask;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, j = lane & 3;
@@ -145,9 +149,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
 
         // start the KV gather before touching q
         int64_t slot_next = fetch_slot(p, pages, t0, t1, warp, lane);
-        issue_rows<kFp8>(p, sRaw, slot_next, warp, lane);
+        issue_rows<kFp8>(p, sRaw, slot_next, sMask, warp, lane);
         slot_next = fetch_slot(p, pages, t0 + kT, t1, warp, lane);
-        issue_rows<kFp8>(p, sRaw + kT * S::kRawRow, slot_next, warp, lane);
+        issue_rows<kFp8>(p, sRaw + kT * S::kRawRow, slot_next, sMask + kT, warp, lane);
         slot_next = fetch_slot(p, pages, t0 + 2 * kT, t1, warp, lane);
 
         // ---- q rows of this head group -> sQ (16-bit), score multipliers
@@ -228,8 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
                     d[1] = make_uint4(h[4], h[5], h[6], h[7]);
                 }
                 __syncthreads();                                     // (B) f16 tile ready
-                if (it + 2 < n_tiles) issue_rows<kFp8>(p, raw, slot_next, warp, lane);
-                else cp_async_commit();
+                if (it + 2 < n_tiles)
+                    issue_rows<kFp8>(p, raw, slot_next, sMask + ((it + 2) & 3) * kT, warp, lane);
+                else
+                    cp_async_commit();
                 slot_next = fetch_slot(p, pages, t0 + (it + 3) * kT, t1, warp, lane);
                 kv = sKvF16;
             } else {
@@ -252,13 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
 
             // ---- online softmax (log2 domain)
             const int n_valid = min(kT, t1 - t0 - it * kT);
+            const uint8_t* tile_mask = sMask + (it & 3) * kT;
             const float c_lo = sCoef[g], c_hi = sCoef[g + 8];
             float s_lo[4], s_hi[4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
-                    const bool ok = 16 * warp + 8 * nt + 2 * j + e < n_valid;
+                    const int tok = 16 * warp + 8 * nt + 2 * j + e;
+                    const bool ok = tok < n_valid && tile_mask[tok];
                     s_lo[2 * nt + e] = ok ? sacc[nt][e] * c_lo : -INFINITY;
                     s_hi[2 * nt + e] = ok ? sacc[nt][2 + e] * c_hi : -INFINITY;
                 }
@@ -327,8 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
             }
             if constexpr (!kFp8) {
                 __syncthreads();                                     // (E) raw stage free
-                if (it + 2 < n_tiles) issue_rows<kFp8>(p, raw, slot_next, warp, lane);
-                else cp_async_commit();
+                if (it + 2 < n_tiles)
+                    issue_rows<kFp8>(p, raw, slot_next, sMask + ((it + 2) & 3) * kT, warp, lane);
+                else
+                    cp_async_commit();
                 slot_next = fetch_slot(p, pages, t0 + (it + 3) * kT, t1, warp, lane);
             }
         }
@@ -351,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
             L_lo += sL[w * kHeadsPerCta + g];
             L_hi += sL[w * kHeadsPerCta + g + 8];
         }
-        const float vscale = kFp8 ? p.k_scale : 1.f;
+        const float vscale = p.k_scale;             // v_t = value * k_scale for both pool types
         const float inv_lo = L_lo > 0.f ? vscale / L_lo : 0.f;
         const float inv_hi = L_hi > 0.f ? vscale / L_hi : 0.f;
         const int h_lo = head0 + g, h_hi = head0 + g + 8;

@@ -1,0 +1,142 @@
+// Blackwell (sm_100 family) tensor-core plumbing: tcgen05 MMA / TMEM,
+// shared-memory matrix descriptors, mbarriers with bounded waits.
+//
+// Conventions used by the kernels:
+//  * UMMA operands live in shared memory in the canonical layouts:
+//      K-major, 128-byte swizzle: rows of 128 B, atoms of 8 rows (1 KB),
+//        16-byte chunk c of row r stored at chunk c ^ (r & 7);
+//        descriptor SBO = stride between 8-row groups, LBO unused;
+//      MN-major, 128-byte swizzle: the same bytes read with M along the
+//        128-byte row and K along rows (SBO = stride between 8-row groups
+//        along K, LBO = stride between 128-byte column blocks along M);
+//      MN-major, no swizzle: core matrices of 8 K-rows x 16 bytes
+//        (LBO = stride between 8-row groups along K).
+//  * every wait on an mbarrier gives up after a time limit, reports it in the
+//    library's flag word and lets the caller unwind (no unbounded spin).
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mla {
+namespace tc {
+
+// ------------------------------------------------------------- descriptors
+
+enum Swizzle : uint64_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4, kSwizzle32B = 6 };
+
+// Shared-memory matrix descriptor (sm_100 tcgen05 format).
+MLA_DEVINLINE uint64_t smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                 Swizzle swz) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;                                  // descriptor version for sm_100
+    d |= static_cast<uint64_t>(swz) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 x E4M3 -> F32.
+// a_mn / b_mn select MN-major operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4)                                  // D format: F32
+           | (0u << 7) | (0u << 10)                   // A, B format: E4M3
+           | (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16)
+           | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+MLA_DEVINLINE void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n"
+                 :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+MLA_DEVINLINE void tmem_dealloc(uint32_t taddr, uint32_t ncols) {     // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n"
+                 :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+MLA_DEVINLINE void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05.mma issued so far by this thread
+// has completed.
+MLA_DEVINLINE void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+
+MLA_DEVINLINE void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+MLA_DEVINLINE void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// Generic-proxy smem writes -> visible to the tensor core (async proxy).
+MLA_DEVINLINE void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
+// 32 lanes x 16 columns of 32-bit TMEM cells: thread t gets lane (base + t).
+MLA_DEVINLINE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+MLA_DEVINLINE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------- mbarrier
+
+MLA_DEVINLINE void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+MLA_DEVINLINE void mbar_fence_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+MLA_DEVINLINE void mbar_arrive(uint64_t* bar) {
+    asm volatile("{\n .reg .b64 st;\n mbarrier.arrive.shared::cta.b64 st, [%0];\n}\n"
+                 :: "r"(smem_u32(bar)) : "memory");
+}
+// Arrives on `bar` once all cp.async operations of this thread have landed.
+MLA_DEVINLINE void mbar_arrive_cp_async(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" :: "r"(smem_u32(bar)) : "memory");
+}
+MLA_DEVINLINE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+MLA_DEVINLINE uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Waits for the phase with the given parity to complete.  Gives up after
+// `limit_ns` (or at once if *abort is already set), sets *abort and the
+// MLA_FLAG_WAIT_TIMEOUT flag, and returns false.
+MLA_DEVINLINE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags,
+                             uint64_t limit_ns = 2000000000ull) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (global_ns() - t0 > limit_ns) {
+            *abort = 1;
+            raise_flag(flags, MLA_FLAG_WAIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+}  // namespace tc
+}  // namespace mla

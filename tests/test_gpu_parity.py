@@ -51,7 +51,7 @@ def test_store_bitexact_on_every_bf16_pattern(k_scale):
 def test_store_separate_padded_pools_and_oob_slot():
     g = np.random.default_rng(2)
     n, P = 37, 90
-    lat = bf16_bits(torch.randn(n, 576) * 0.3)
+    lat = bf16_bits((torch.randn(n, 576) * 0.3).to(torch.bfloat16))
     slots = g.permutation(P)[:n].astype(np.int64)
     slots[5] = P                                    # out of range: skipped and flagged
     ckv0 = W.random_fill_bytes(g, (P, 544))         # row stride 544
