@@ -145,6 +145,41 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q_stride_b,
                             void* workspace, size_t workspace_bytes,
                             void* stream);
 
+/*
+ * mla_decode_run_static_scratch -- mla_decode_run for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this call.
+ *
+ * Some callers have no way to hand the decode a workspace: a plugin inside a
+ * framework that owns every GPU allocation, a real-time loop that must not
+ * pay cudaMalloc's implicit device synchronisation, code that must not touch
+ * the allocator between steps.  This call takes the same arguments as
+ * mla_decode_run minus the workspace and keeps the split-KV partials in a
+ * fixed array of MLA_STATIC_SCRATCH_BYTES compiled into the library; the
+ * call allocates nothing (the plan is built beforehand by mla_decode_plan).
+ *  - The array exists once per GPU that loads the library and stays
+ *    allocated until the process exits.
+ *  - The first call on a device looks up the array's device address; make
+ *    that first call before any stream capture begins.
+ *  - Every call shares the array: calls whose GPU work overlaps (other
+ *    streams, other host threads) race on it.  Calls on one stream are
+ *    ordered.  Nothing in the array needs to start at zero.
+ * Errors: as mla_decode_run; MLA_ERR_WORKSPACE if the plan needs more than
+ * MLA_STATIC_SCRATCH_BYTES of scratch (see mla_decode_plan_info).
+ */
+#define MLA_STATIC_SCRATCH_BYTES (8u << 20)
+mla_status_t mla_decode_run_static_scratch(mla_plan_t plan, const void* q,
+                                           int64_t q_stride_b, int64_t q_stride_h,
+                                           const void* ckv_pool,
+                                           int64_t ckv_row_stride_bytes,
+                                           const void* kpe_pool,
+                                           int64_t kpe_row_stride_bytes,
+                                           int64_t num_pool_slots,
+                                           const int32_t* kv_indptr_dev,
+                                           const int32_t* kv_indices_dev,
+                                           const int32_t* seq_lens_dev, float k_scale,
+                                           float softmax_scale, void* out, float* lse,
+                                           void* stream);
+
 /* Releases a plan and its device / pinned buffers (after the caller has
  * synchronised any stream still using it).  NULL is accepted. */
 mla_status_t mla_decode_plan_destroy(mla_plan_t plan);

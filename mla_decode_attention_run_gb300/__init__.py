@@ -17,12 +17,14 @@ __all__ = [
     "MLA_KV_FP8_E4M3", "MLA_KV_BF16", "MLAError", "library", "library_path",
     "mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy", "mla_decode_plan_info",
     "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast", "mla_get_last_error",
-    "exported_symbols", "D_CKV", "D_KPE", "D_QK",
+    "exported_symbols", "D_CKV", "D_KPE", "D_QK", "mla_decode_run_static_scratch",
+    "STATIC_SCRATCH_BYTES",
 ]
 
 D_CKV, D_KPE, D_QK = 512, 64, 576
 MLA_KV_FP8_E4M3, MLA_KV_BF16 = 0, 1
 FLAG_INDEX_OOB, FLAG_PLAN_MISMATCH, FLAG_WAIT_TIMEOUT = 0x1, 0x2, 0x4
+STATIC_SCRATCH_BYTES = 8 << 20       # MLA_STATIC_SCRATCH_BYTES
 
 library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmla_decode.so")
 _lib = None
@@ -54,6 +56,8 @@ def library():
                                     ctypes.POINTER(_sz), _P]
     lib.mla_decode_run.argtypes = [_P, _P, _i64, _i64, _P, _i64, _P, _i64, _i64, _P, _P, _P, _f32,
                                    _f32, _P, _P, _P, _sz, _P]
+    lib.mla_decode_run_static_scratch.argtypes = [_P, _P, _i64, _i64, _P, _i64, _P, _i64, _i64,
+                                                  _P, _P, _P, _f32, _f32, _P, _P, _P]
     lib.mla_decode_plan_destroy.argtypes = [_P]
     lib.mla_decode_plan_info.argtypes = [_P, _PI32, _PI32, _PI32, ctypes.POINTER(_sz)]
     lib.mla_decode_schedule.argtypes = [_P, _P, _i32, _i32, _i32, ctypes.c_int, _i32, _P, _i32,
@@ -65,7 +69,7 @@ def library():
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
                  "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
-                 "mla_get_last_error"):
+                 "mla_get_last_error", "mla_decode_run_static_scratch"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -78,7 +82,7 @@ def exported_symbols() -> list[str]:
     names = []
     for n in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
               "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
-              "mla_get_last_error", "mla_status_string"):
+              "mla_get_last_error", "mla_status_string", "mla_decode_run_static_scratch"):
         getattr(lib, n)
         names.append(n)
     return names
@@ -158,6 +162,22 @@ def mla_decode_run(plan: Plan, q, ckv_pool, kpe_pool, num_pool_slots: int, kv_in
                               seq_lens_dev.data_ptr(), k_scale, softmax_scale, out.data_ptr(),
                               lse.data_ptr(), _dptr(workspace), ws_bytes, _stream(stream)),
            "mla_decode_run")
+
+
+def mla_decode_run_static_scratch(plan: Plan, q, ckv_pool, kpe_pool, num_pool_slots: int,
+                                  kv_indptr_dev, kv_indices_dev, seq_lens_dev, k_scale: float,
+                                  softmax_scale: float, out, lse, stream=None):
+    """mla_decode_run without a workspace argument, for callers that cannot
+    allocate device memory: the split-KV partials go to a fixed array inside
+    the library (STATIC_SCRATCH_BYTES per GPU, kept until exit).  Calls that
+    overlap on the GPU share that array and race; calls on one stream are
+    ordered.  Raises MLAError (status 3) if the plan needs more scratch."""
+    _check(library().mla_decode_run_static_scratch(
+        plan.handle, q.data_ptr(), q.stride(0), q.stride(1), ckv_pool.data_ptr(),
+        _row_stride_bytes(ckv_pool), kpe_pool.data_ptr(), _row_stride_bytes(kpe_pool),
+        num_pool_slots, kv_indptr_dev.data_ptr(), _dptr(kv_indices_dev),
+        seq_lens_dev.data_ptr(), k_scale, softmax_scale, out.data_ptr(), lse.data_ptr(),
+        _stream(stream)), "mla_decode_run_static_scratch")
 
 
 def mla_decode_plan_destroy(plan: Plan):
