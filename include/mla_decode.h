@@ -195,8 +195,9 @@ mla_status_t mla_decode_plan_info(mla_plan_t plan, int32_t* num_ctas,
  * plan with these arguments would use on a GPU with `num_sms` SMs.  Writes
  * up to `capacity` segments as int32 quintuples
  *     (cta, request, token_begin, token_end, partial_index or -1)
- * into segments_out (may be NULL), in launch order.  Validates exactly like
- * mla_decode_plan.
+ * into segments_out (may be NULL), in launch order; tile_tokens receives the
+ * kernel's tile (segments start on tile boundaries).  Validates exactly like
+ * mla_decode_plan.  Output pointers may be NULL.
  */
 mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
                                  const int32_t* seq_lens_host, int32_t batch,
@@ -204,7 +205,8 @@ mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
                                  mla_kv_dtype_t kv_dtype, int32_t num_sms,
                                  int32_t* segments_out, int32_t capacity,
                                  int32_t* num_segments, int32_t* num_partials,
-                                 int32_t* num_ctas, size_t* workspace_bytes);
+                                 int32_t* num_ctas, int32_t* tile_tokens,
+                                 size_t* workspace_bytes);
 
 /*
  * kv_store_fp8 -- quantize-on-store scatter ([P1] "Step 3", CastToFP8 in

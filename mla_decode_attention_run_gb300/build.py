@@ -18,7 +18,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmla_decode.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["runtime.cu", "kv_cache.cu", "plan.cu", "decode.cu", "decode_static.cu"]
+SOURCES = ["runtime.cu", "kv_cache.cu", "plan.cu", "decode.cu", "decode_tc.cu",
+           "decode_static.cu"]
 
 
 def _nvcc() -> str:

@@ -27,6 +27,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "decode_params.h"
 #include "plan.h"
 
 namespace mla {
@@ -52,27 +53,7 @@ struct Smem {
     static constexpr size_t kBytes = kMask + size_t(4) * kT;
 };
 
-struct DecodeParams {
-    const uint16_t* q;
-    int64_t q_sb, q_sh;
-    const uint8_t* ckv;
-    int64_t ckv_stride;
-    const uint8_t* kpe;
-    int64_t kpe_stride;
-    int64_t num_slots;
-    const int32_t* indptr;
-    const int32_t* indices;
-    const int32_t* seq_lens;
-    int32_t page_size, heads, head_groups;
-    float k_scale, softmax_scale;
-    uint16_t* out;
-    float* lse;
-    float* part_o;
-    float* part_lse;
-    const int32_t* cta_ptr;
-    const int32_t* segs;
-    uint32_t* flags;
-};
+
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -537,7 +518,9 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
     p.segs = plan->dev_meta + plan->off_segs;
     p.flags = device_flags_ptr();
 
-    if (s.num_ctas > 0) {
+    if (s.num_ctas > 0 && s.kernel == DecodeKernel::kTc) {
+        if (launch_decode_tc(p, s.num_ctas, cs) != cudaSuccess) return MLA_ERR_CUDA;
+    } else if (s.num_ctas > 0) {
         const dim3 grid(s.num_ctas * s.head_groups);
         cudaError_t e;
         if (fp8) {

@@ -1,0 +1,34 @@
+// Launch parameters shared by the decode kernels (decode.cu, decode_tc.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mla {
+
+struct DecodeParams {
+    const uint16_t* q;          // BF16 [B][H][576] with strides q_sb / q_sh (elements)
+    int64_t q_sb, q_sh;
+    const uint8_t* ckv;         // row `slot` at ckv + slot * ckv_stride
+    int64_t ckv_stride;
+    const uint8_t* kpe;
+    int64_t kpe_stride;
+    int64_t num_slots;
+    const int32_t* indptr;
+    const int32_t* indices;
+    const int32_t* seq_lens;
+    int32_t page_size, heads, head_groups;
+    float k_scale, softmax_scale;
+    uint16_t* out;              // BF16 [B][H][512]
+    float* lse;                 // [B][H], natural log
+    float* part_o;              // split-KV partials: [partials][H][512] fp32 (normalised)
+    float* part_lse;            // [partials][H]
+    const int32_t* cta_ptr;     // plan: segments of CTA c are [cta_ptr[c], cta_ptr[c+1])
+    const int32_t* segs;        // plan: 4 ints per segment: request, t0, t1, partial (-1 final)
+    uint32_t* flags;            // library flag word
+};
+
+// Launches the tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` CTAs.
+cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream);
+
+}  // namespace mla

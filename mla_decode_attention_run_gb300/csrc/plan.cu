@@ -19,12 +19,18 @@ bool heads_supported(int32_t h) { return (h >= 1 && h <= 16) || (h > 16 && h <= 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Resident decode CTAs per SM for a plan (the kernel's shared-memory budget
-// allows one).
-int ctas_per_sm(mla_kv_dtype_t) { return 1; }
+// Resident decode CTAs per SM (both kernels' shared-memory budgets allow one).
+int ctas_per_sm(DecodeKernel) { return 1; }
+
+// The tcgen05 kernel covers FP8 pools with up to 16 heads; the mma.sync
+// kernel everything else (more heads in groups of 16, BF16 pools).
+DecodeKernel pick_kernel(mla_kv_dtype_t dtype, int32_t heads) {
+    return (dtype == MLA_KV_FP8_E4M3 && heads <= kHeadsPerCta) ? DecodeKernel::kTc
+                                                               : DecodeKernel::kMma;
+}
 
 // A CTA gets at least this many tiles when there is enough work.
-constexpr int64_t kMinTilesPerCta = 2;
+int64_t min_tiles_per_cta(DecodeKernel k) { return k == DecodeKernel::kTc ? 1 : 2; }
 
 }  // namespace
 
@@ -48,10 +54,12 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
     const mla_status_t st = validate_plan_inputs(indptr, seq, B, H, ps, dtype);
     if (st != MLA_OK) return st;
     if (num_sms < 1) return MLA_ERR_INVALID_ARG;
+    const DecodeKernel kernel = pick_kernel(dtype, H);
+    const int64_t tile = kernel == DecodeKernel::kTc ? kTcTileTokens : kTileTokens;
     int64_t n_tokens = 0, n_tiles = 0;
     for (int32_t b = 0; b < B; ++b) {
         n_tokens += seq[b];
-        n_tiles += (seq[b] + kTileTokens - 1) / kTileTokens;
+        n_tiles += (seq[b] + tile - 1) / tile;
     }
 
     s = Schedule();
@@ -59,19 +67,21 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
     s.heads = H;
     s.page_size = ps;
     s.kv_dtype = dtype;
+    s.kernel = kernel;
+    s.tile_tokens = static_cast<int32_t>(tile);
     s.n_tokens = n_tokens;
     s.head_groups = (H + kHeadsPerCta - 1) / kHeadsPerCta;
 
-    int64_t ctas = static_cast<int64_t>(num_sms) * ctas_per_sm(dtype) / s.head_groups;
+    int64_t ctas = static_cast<int64_t>(num_sms) * ctas_per_sm(kernel) / s.head_groups;
     if (ctas < 1) ctas = 1;
-    const int64_t by_work = (n_tiles + kMinTilesPerCta - 1) / kMinTilesPerCta;
+    const int64_t by_work = (n_tiles + min_tiles_per_cta(kernel) - 1) / min_tiles_per_cta(kernel);
     if (ctas > by_work) ctas = by_work;
     s.num_ctas = static_cast<int32_t>(ctas);
 
     // request tile offsets in the concatenated tile list
     std::vector<int64_t> first_tile(B + 1, 0);
     for (int32_t b = 0; b < B; ++b)
-        first_tile[b + 1] = first_tile[b] + (seq[b] + kTileTokens - 1) / kTileTokens;
+        first_tile[b + 1] = first_tile[b] + (seq[b] + tile - 1) / tile;
 
     std::vector<int32_t> segs_per_req(B, 0);
     s.cta_ptr.assign(s.num_ctas + 1, 0);
@@ -83,8 +93,8 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
         while (pos < hi) {
             while (first_tile[b + 1] <= pos) ++b;       // skips empty requests too
             const int64_t end = hi < first_tile[b + 1] ? hi : first_tile[b + 1];
-            const int64_t t0 = (pos - first_tile[b]) * kTileTokens;
-            int64_t t1 = (end - first_tile[b]) * kTileTokens;
+            const int64_t t0 = (pos - first_tile[b]) * tile;
+            int64_t t1 = (end - first_tile[b]) * tile;
             if (t1 > seq[b]) t1 = seq[b];
             s.segs.insert(s.segs.end(), {b, static_cast<int32_t>(t0), static_cast<int32_t>(t1), -1});
             ++segs_per_req[b];
@@ -124,7 +134,8 @@ extern "C" mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
                                             mla_kv_dtype_t kv_dtype, int32_t num_sms,
                                             int32_t* segments_out, int32_t capacity,
                                             int32_t* num_segments, int32_t* num_partials,
-                                            int32_t* num_ctas, size_t* workspace_bytes) {
+                                            int32_t* num_ctas, int32_t* tile_tokens,
+                                            size_t* workspace_bytes) {
     Schedule s;
     const mla_status_t st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads,
                                                 page_size, kv_dtype, num_sms, s);
@@ -142,6 +153,7 @@ extern "C" mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
     if (num_segments) *num_segments = s.n_segs();
     if (num_partials) *num_partials = s.n_partials;
     if (num_ctas) *num_ctas = s.num_ctas;
+    if (tile_tokens) *tile_tokens = s.tile_tokens;
     if (workspace_bytes) *workspace_bytes = s.workspace_bytes;
     return MLA_OK;
 }

@@ -10,9 +10,17 @@
 
 namespace mla {
 
-// Tokens per KV tile of the decode kernel, and heads per CTA.
+// Tokens per KV tile of the mma.sync decode kernel, of the tcgen05 decode
+// kernel, and heads per CTA.
 constexpr int kTileTokens = 64;
+constexpr int kTcTileTokens = 128;
 constexpr int kHeadsPerCta = 16;
+
+// Which decode kernel a plan launches.
+enum class DecodeKernel : int32_t {
+    kMma = 0,   // mma.sync, E4M3 widened to f16 in smem; also the BF16-pool kernel
+    kTc = 1,    // tcgen05 kind::f8f6f4 on the E4M3 bytes in place (FP8, H <= 16)
+};
 
 // The split-KV schedule.  The concatenation of all requests' tiles is cut
 // into `num_ctas` contiguous, equal-sized (+-1 tile) ranges; each range is a
@@ -23,6 +31,8 @@ constexpr int kHeadsPerCta = 16;
 struct Schedule {
     int32_t batch = 0, heads = 0, page_size = 0;
     mla_kv_dtype_t kv_dtype = MLA_KV_FP8_E4M3;
+    DecodeKernel kernel = DecodeKernel::kMma;
+    int32_t tile_tokens = kTileTokens;
     int32_t head_groups = 0;
     int32_t num_ctas = 0;            // token ranges; grid = num_ctas * head_groups
     std::vector<int32_t> cta_ptr;    // [num_ctas + 1] -> segment index

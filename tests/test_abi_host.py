@@ -51,7 +51,8 @@ def _indptr(lens, ps):
 
 def _check_schedule(segs, info, lens, heads, num_sms=152):
     lens = np.asarray(lens)
-    tile = 64
+    tile = info["tile_tokens"]
+    assert tile in (64, 128)
     # every request's tokens are covered exactly once, in order
     for b in range(len(lens)):
         mine = segs[segs[:, 1] == b]
@@ -109,6 +110,15 @@ def test_schedule_ragged_and_empty_requests():
     lens = np.array([0, 1, 63, 64, 65, 0, 1000, 3])
     segs, info = M.mla_decode_schedule(_indptr(lens, 3), lens, len(lens), 4, 3, num_sms=5)
     _check_schedule(segs, info, lens, 4, num_sms=5)
+
+
+def test_schedule_picks_the_fp8_tensor_core_kernel_for_small_head_counts():
+    lens = np.array([1000, 3000])
+    _, fp8_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_FP8_E4M3)
+    _, bf16_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_BF16)
+    _, fp8_32 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 32, 1, M.MLA_KV_FP8_E4M3)
+    assert fp8_16["tile_tokens"] == 128
+    assert bf16_16["tile_tokens"] == 64 and fp8_32["tile_tokens"] == 64
 
 
 def test_schedule_all_empty():

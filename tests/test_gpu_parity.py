@@ -323,3 +323,21 @@ def test_full_pool_cast_then_bf16_decode():
     o_ref, lse_ref = oracle.decode_fp8(w.q_bf16, pool_np[:, :512], pool_np[:, 512:], w.kv_indptr,
                                        w.kv_indices, w.seq_lens, 1, w.k_scale, w.softmax_scale)
     check_attention(out, lse, o_ref, lse_ref, "full-pool cast")
+
+
+def test_fp8_tensor_core_path_precision():
+    """The FP8 tensor-core kernel (E4M3 cache bytes as MMA operands, q and P
+    each split exactly into two E4M3 terms) is checked against the oracle at
+    a bound four times tighter than the contract: a lost second term (about
+    2^-5 relative in P, 2^-4 in q) would fail it."""
+    w = W.make_workload("concurrency", batch=12, num_slots=W.POOL_SLOTS, seed=31)
+    segs, info = M.mla_decode_schedule(w.kv_indptr, w.seq_lens, w.batch, w.heads, 1)
+    assert info["tile_tokens"] == 128                # the tcgen05 kernel serves this plan
+    pool = oracle_pool(w)
+    out, lse, flags = _decode_case(w, pool)
+    assert flags == 0
+    o_ref, lse_ref = oracle.decode_fp8(w.q_bf16, pool[:, :512], pool[:, 512:], w.kv_indptr,
+                                       w.kv_indices, w.seq_lens, 1, w.k_scale, w.softmax_scale)
+    o = out.float().cpu().numpy()
+    assert np.all(np.abs(o - o_ref) <= 2.5e-3 + 2.5e-3 * np.abs(o_ref))
+    assert np.all(np.abs(lse.cpu().numpy() - lse_ref) <= 2.5e-4)
