@@ -518,6 +518,7 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
     p.segs = plan->dev_meta + plan->off_segs;
     p.flags = device_flags_ptr();
 
+    if (s.kernel == DecodeKernel::kTc && num_pool_slots >= INT32_MAX) return MLA_ERR_UNSUPPORTED;
     if (s.num_ctas > 0 && s.kernel == DecodeKernel::kTc) {
         if (launch_decode_tc(p, s.num_ctas, cs) != cudaSuccess) return MLA_ERR_CUDA;
     } else if (s.num_ctas > 0) {

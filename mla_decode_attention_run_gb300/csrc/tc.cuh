@@ -114,6 +114,33 @@ MLA_DEVINLINE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
+// Non-blocking test of a phase.
+MLA_DEVINLINE bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Arrives on `bar` and adds `bytes` to the transaction count its phase waits for.
+MLA_DEVINLINE void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n"
+                 :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// TMA gather of four rows (row coordinates r0..r3, starting column x) of a
+// 2-D tensor map into consecutive box rows at `dst`; completes on `bar`.
+MLA_DEVINLINE void tma_gather4(uint32_t dst, const void* tensor_map, int32_t x, int32_t r0,
+                               int32_t r1, int32_t r2, int32_t r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n"
+        :: "r"(dst), "l"(tensor_map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+           "r"(smem_u32(bar))
+        : "memory");
+}
+
 MLA_DEVINLINE uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
