@@ -31,11 +31,12 @@
 //
 // Warp roles (one CTA per SM, persistent over its token range):
 //   warps 0-1  gather the tile's rows into a 2-stage ring, split between
-//              two engines: warp 0 uses TMA tile::gather4 (four pool rows
-//              per instruction, c_kv channels 0..255, 128-byte swizzle,
-//              out-of-range rows zero-filled), warp 1 16-byte cp.async
-//              (channels 256..511 and the 64 k_pe channels, 64-byte
-//              swizzle); both complete on the stage's mbarrier;
+//              two engines by their measured rates: warp 0 uses TMA
+//              tile::gather4 (four pool rows per instruction, c_kv channels
+//              0..127, 128-byte swizzle, out-of-range rows zero-filled),
+//              warp 1 16-byte cp.async (c_kv channels 128..511 and the 64
+//              k_pe channels, 64-byte swizzle); both complete on the stage's
+//              mbarrier;
 //   warp 2     one thread issues every tcgen05.mma and commit, polling so
 //              that PV of one tile and QK^T of the next go out in whichever
 //              order their inputs become ready;
@@ -143,16 +144,17 @@ __device__ __forceinline__ void wg_bar() { asm volatile("bar.sync 1, 128;\n" :::
 // ------------------------------------------------------------ producer warps
 //
 // Rows of a tile are gathered by two engines at once: the TMA unit (warp 0,
-// tile::gather4, c_kv channels 0..255) and the LSU (warp 1, 16-byte cp.async,
-// c_kv channels 256..511 and k_pe).  Each engine caps the gather requests an
-// SM keeps in flight; using both raises the bytes in flight per SM.
+// tile::gather4: c_kv channels 0..127) and the LSU (warp 1, 16-byte
+// cp.async: c_kv channels 128..511 and k_pe).  Each engine caps the gather
+// requests an SM keeps in flight; measured on GB300, TMA gathers sustain
+// about a quarter of the LSU's rate, so it takes 16 of the tile's 72 KB.
 
 struct TmaMaps {
     CUtensorMap ckv;    // [rows][512] E4M3, box 128 x 1, 128-byte swizzle
     int32_t rows;       // tensor-map height; a row coordinate >= rows reads zeros
 };
 
-constexpr int kTmaBlocks = 2;                                   // c_kv blocks 0, 1 by TMA
+constexpr int kTmaBlocks = 1;                                   // c_kv block 0 by TMA
 constexpr int32_t kNoRow = INT32_MIN;
 constexpr uint32_t kTmaBytes = kTmaBlocks * kBlk;
 
@@ -259,16 +261,19 @@ __device__ void producer_lsu(const DecodeParams& p, uint8_t* base, uint64_t* bar
         if (more) cur.prefetch(p, lane, false);
         if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
         uint8_t* stage = base + kOffStage + slot * kStage;
-        // c_kv channels 256..511: 16 chunks per row, two rows per instruction
-        const int half = lane >> 4, ch = lane & 15;
-        const int cb = kTmaBlocks + (ch >> 3), cc = ch & 7;
+        // c_kv blocks kTmaBlocks..3: 8 chunks (128 B) per row, four rows per
+        // instruction
+        const int r4 = lane >> 3, c8 = lane & 7;
 #pragma unroll
-        for (int rp = 0; rp < kTT / 2; ++rp) {
-            const int row = 2 * rp + half;
-            const int32_t s = __shfl_sync(0xffffffffu, sl[rp >> 4], row & 31);
-            const int64_t ss = s >= 0 ? s : 0;
-            cp_async16(stage + cb * kBlk + row * 128 + ((cc ^ (row & 7)) << 4),
-                       p.ckv + ss * p.ckv_stride + kTmaBlocks * 128 + ch * 16, s >= 0 ? 16u : 0u);
+        for (int cb = kTmaBlocks; cb < 4; ++cb) {
+#pragma unroll
+            for (int j = 0; j < kTT / 4; ++j) {
+                const int row = 4 * j + r4;
+                const int32_t s = __shfl_sync(0xffffffffu, sl[j >> 3], row & 31);
+                const int64_t ss = s >= 0 ? s : 0;
+                cp_async16(stage + cb * kBlk + row * 128 + ((c8 ^ (row & 7)) << 4),
+                           p.ckv + ss * p.ckv_stride + cb * 128 + c8 * 16, s >= 0 ? 16u : 0u);
+            }
         }
         // k_pe: 4 chunks per row, eight rows per instruction (64-byte swizzle)
         const int r8 = lane >> 2, c4 = lane & 3;
