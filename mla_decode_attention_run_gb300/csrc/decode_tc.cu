@@ -23,32 +23,36 @@
 //   S^T[128 x 32]  = K_tile[128 x 576] . [q1;q2]^T    18 MMAs, K-major A/B
 //   O^T[512 x 32] += V^T[512 x 128] . [P1;P2]^T       16 MMAs, MN-major A/B
 // The same swizzled smem tile serves as K-major A (tokens x dims) and
-// MN-major A (dims x tokens); S and O live in TMEM.
+// MN-major A (dims x tokens).  S (double-buffered per tile) and O (one
+// accumulator per segment, double-buffered across segments) live in TMEM.
 //
 // Online softmax with lazy rescaling: the running maximum m only moves when
 // some score exceeds it by more than 2^4 (in log2 units), so most tiles skip
 // the cross-token maximum; p = 2^(s - m) <= 16 and p * 16 still fits E4M3.
+// O accumulates in TMEM across a segment's tiles; when m does move, the
+// softmax warps rescale it in place before the next PV may add to it.
 //
 // Warp roles (one CTA per SM, persistent over its token range):
-//   warps 0-1  gather the tile's rows into a 2-stage ring, split between
-//              two engines by their measured rates: warp 0 uses TMA
-//              tile::gather4 (four pool rows per instruction, c_kv channels
-//              0..127, 128-byte swizzle, out-of-range rows zero-filled),
-//              warp 1 16-byte cp.async (c_kv channels 128..511 and the 64
-//              k_pe channels, 64-byte swizzle); both complete on the stage's
-//              mbarrier;
-//   warp 2     one thread issues every tcgen05.mma and commit, polling so
+//   warp 0     schedules tiles kAhead ahead of the stage fills: resolves each
+//              row's pool slot (or -1: past the context, outside the pool)
+//              into a small shared ring and has L2 prefetch the rows' cache
+//              lines, so the fills below read L2 rather than wait on DRAM;
+//   warps 0-3  fill a 2-stage ring with 16-byte cp.async: warp w copies
+//              c_kv channels 128w .. 128w+127 (128-byte swizzle) and a
+//              quarter of the k_pe rows (64-byte swizzle); an invalid row is
+//              zero-filled.  Measured on GB300, four LSU warps fed from L2
+//              gather at the HBM rate, which neither fewer warps nor TMA
+//              tile::gather4 reach;
+//   warp 4     one thread issues every tcgen05.mma and commit, polling so
 //              that PV of one tile and QK^T of the next go out in whichever
 //              order their inputs become ready;
-//   warp 3     prepares [q1;q2] and the per-head score multipliers for each
+//   warp 5     prepares [q1;q2] and the per-head score multipliers for each
 //              segment (double-buffered; lane = half a head row);
-//   warps 4-7  one thread per TMEM lane: online softmax of a token's 16
-//              heads, the E4M3 split of P, then the O correction (lane =
-//              output channel) and the epilogue.
+//   warps 6-9  one thread per TMEM lane: online softmax of a token's 16
+//              heads and the E4M3 split of P, rescaling O when the maximum
+//              moves, and the epilogue (lane = output channel).
 // Every mbarrier wait is bounded; on a timeout the CTA sets
 // MLA_FLAG_WAIT_TIMEOUT, drains its MMAs and copies, frees TMEM and exits.
-#include <cuda.h>
-
 #include <mutex>
 #include <vector>
 
@@ -65,7 +69,9 @@ using namespace tc;
 constexpr int kTT = kTcTileTokens;          // 128 tokens per tile (MMA M)
 constexpr int kM = 128;
 constexpr int kStages = 2;
-constexpr int kThreads = 256;
+constexpr int kFillWarps = 4;
+constexpr int kWarpMma = 4, kWarpQ = 5, kWarpWg = 6;
+constexpr int kThreads = 320;
 constexpr int kBlk = kTT * 128;             // 128 rows x 128 B, 128-byte swizzle (128 c_kv channels)
 constexpr int kRope = kTT * 64;             // 128 rows x 64 B, 64-byte swizzle (the 64 k_pe channels)
 constexpr int kStage = 4 * kBlk + kRope;    // 72 KB per tile
@@ -76,19 +82,25 @@ constexpr int kPUnit = kTT * 16;            // one E4M3 term of P^T: 128 tokens 
 constexpr int kPBytes = 2 * kPUnit;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;               // S[j]: columns 32j .. 32j+31
-constexpr uint32_t kColO = 64;              // O[j]: 64 + 128j + 32mb (mb = 128-channel block)
+constexpr uint32_t kColO = 64;              // O[b]: 64 + 128b + 32mb (mb = 128-channel block)
 constexpr int kKSteps = kDQk / 32;          // 18 k-steps of 32 channels for QK
 constexpr float kTau = 4.f;                 // lazy-rescale threshold (log2 units)
 constexpr float kPScale = 16.f;             // P is stored as p * 2^kTau
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kRing = 8;                    // scheduled tiles' slot lists in flight
+constexpr int kAhead = 2;                   // tiles scheduled (and prefetched) beyond the one filling
+static_assert(kAhead + kStages < kRing, "the scheduler may not lap the softmax warps");
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffStage = 0;
 constexpr int kOffQ = kOffStage + kStages * kStage;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kOffRed = kOffBar + 256;      // tile maxima: 2 x 4 warps x 16
+constexpr int kOffRing = kOffP + 2 * kPBytes;   // kRing x 128 slots (int32)
+constexpr int kOffQRaw = kOffRing + kRing * kTT * 4;   // BF16 q rows of one request
+constexpr int kQRawRow = kDQk * 2 + 16;   // padded: consecutive heads start 4 banks apart
+constexpr int kOffBar = kOffQRaw + kHeadsPerCta * kQRawRow;
+constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x 16
 constexpr int kOffLsum = kOffRed + 512;     // softmax denominators: 4 warps x 16
 constexpr int kOffCoef = kOffLsum + 256;    // score multipliers: 2 x 16
 constexpr int kOffFlag = kOffCoef + 128;    // rescale votes: 2 x 4 warps
@@ -98,13 +110,15 @@ static_assert(kBlk % 1024 == 0 && kStage % 1024 == 0 && kQBytes % 1024 == 0,
               "swizzle atoms need 1 KB alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTT == kM, "a tile fills the MMA's M exactly");
+static_assert(kThreads == 32 * (kWarpWg + 4), "four softmax warps after the others");
 
 enum : int {
     KV_FULL = 0, KV_EMPTY = kStages, S_FULL = 2 * kStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
-    O_FULL = P_FULL + 2, O_FREE = O_FULL + 2, Q_FULL = O_FREE + 2, Q_FREE = Q_FULL + 2,
-    DONE = Q_FREE + 2, NUM_BARS = DONE + 1
+    PV_DONE = P_FULL + 2, O_FREE = PV_DONE + 2, Q_FULL = O_FREE + 2, Q_FREE = Q_FULL + 2,
+    DONE = Q_FREE + 2, Q_RAW = DONE + 1, SL_FULL = Q_RAW + 1, SL_EMPTY = SL_FULL + kRing,
+    NUM_BARS = SL_EMPTY + kRing
 };
-static_assert(NUM_BARS == 19, "barrier count table below assumes two stages");
+static_assert(NUM_BARS == 36 && NUM_BARS * 8 <= 512, "barrier count table below assumes two stages");
 
 struct Seg {
     int32_t b, t0, t1, part, ntiles;
@@ -122,16 +136,10 @@ __device__ __forceinline__ Seg load_seg(const DecodeParams& p, int si) {
     return s;
 }
 
-__device__ __forceinline__ int64_t token_slot(const DecodeParams& p, const int32_t* pages, int32_t t,
-                                              int32_t t_end, bool flag) {
-    if (t >= t_end) return -1;
-    const int64_t page = pages[p.page_size == 1 ? t : t / p.page_size];
-    const int64_t slot = p.page_size == 1 ? page : page * p.page_size + t % p.page_size;
-    if (page < 0 || slot >= p.num_slots) {
-        if (flag) raise_flag(p.flags, MLA_FLAG_INDEX_OOB);
-        return -1;
-    }
-    return slot;
+__device__ __forceinline__ int count_tiles(const DecodeParams& p, int lo, int hi) {
+    int n = 0;
+    for (int si = lo; si < hi; ++si) n += load_seg(p, si).ntiles;
+    return n;
 }
 
 __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
@@ -143,29 +151,21 @@ __device__ __forceinline__ void wg_bar() { asm volatile("bar.sync 1, 128;\n" :::
 
 // ------------------------------------------------------------ producer warps
 //
-// Rows of a tile are gathered by two engines at once: the TMA unit (warp 0,
-// tile::gather4: c_kv channels 0..127) and the LSU (warp 1, 16-byte
-// cp.async: c_kv channels 128..511 and k_pe).  Each engine caps the gather
-// requests an SM keeps in flight; measured on GB300, TMA gathers sustain
-// about a quarter of the LSU's rate, so it takes 16 of the tile's 72 KB.
+// Warp 0 walks the CTA's tiles kAhead ahead of the stage fills: it resolves
+// the 128 rows of a tile to pool slots, publishes them in a shared ring
+// (SL_FULL / SL_EMPTY) and has L2 prefetch each row's cache lines.  By the
+// time a stage frees up, the rows it needs are on their way to (or already
+// in) L2, so a stage is held for an L2 round trip rather than a DRAM one.
 
-struct TmaMaps {
-    CUtensorMap ckv;    // [rows][512] E4M3, box 128 x 1, 128-byte swizzle
-    int32_t rows;       // tensor-map height; a row coordinate >= rows reads zeros
-};
-
-constexpr int kTmaBlocks = 1;                                   // c_kv block 0 by TMA
 constexpr int32_t kNoRow = INT32_MIN;
-constexpr uint32_t kTmaBytes = kTmaBlocks * kBlk;
 
-// Cursor over the tiles of a CTA's segments, with the raw page entries of up
-// to four rows per lane for one tile: rows lane + 32q (LSU warp) or 4 lane + q
-// (TMA warp, whose gather4 takes four consecutive rows).
+// Cursor over the tiles of a CTA's segments, with the raw page entries of
+// rows 4 lane .. 4 lane + 3 of one tile.
 struct TileCursor {
     int si, seg_hi, it;
     Seg sg;
     const int32_t* pages;
-    int32_t pg[4];                      // page entry, or kNoRow past the context / tile
+    int32_t pg[4];                      // page entry, or kNoRow past the context
     int32_t t[4];                       // token index of each row
 
     __device__ void init(const DecodeParams& p, int lo, int hi) {
@@ -178,23 +178,21 @@ struct TileCursor {
     __device__ bool valid() const { return si < seg_hi; }
     // issue the (independent) index loads of the current tile; nothing waits
     // on them until rows() is called
-    __device__ void prefetch(const DecodeParams& p, int lane, bool consecutive) {
+    __device__ void prefetch(const DecodeParams& p, int lane) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int row = consecutive ? 4 * lane + q : lane + 32 * q;
-            t[q] = sg.t0 + it * kTT + row;
-            pg[q] = (row < kTT && t[q] < sg.t1) ? pages[p.page_size == 1 ? t[q] : t[q] / p.page_size]
-                                                : kNoRow;
+            t[q] = sg.t0 + it * kTT + 4 * lane + q;
+            pg[q] = t[q] < sg.t1 ? pages[p.page_size == 1 ? t[q] : t[q] / p.page_size] : kNoRow;
         }
     }
-    // slot of each row, or -1 (past the context or the tile, or outside the pool)
-    __device__ void rows(const DecodeParams& p, int32_t (&slot)[4], bool flag) const {
+    // slot of each row, or -1 (past the context or outside the pool: flagged)
+    __device__ void rows(const DecodeParams& p, int32_t (&slot)[4]) const {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int64_t s = p.page_size == 1 ? int64_t(pg[q])
                                                : int64_t(pg[q]) * p.page_size + t[q] % p.page_size;
             const bool ok = pg[q] >= 0 && s < p.num_slots;
-            if (!ok && pg[q] != kNoRow && flag) raise_flag(p.flags, MLA_FLAG_INDEX_OOB);
+            if (!ok && pg[q] != kNoRow) raise_flag(p.flags, MLA_FLAG_INDEX_OOB);
             slot[q] = ok ? static_cast<int32_t>(s) : -1;
         }
     }
@@ -208,83 +206,102 @@ struct TileCursor {
     }
 };
 
-__device__ void producer_tma(const DecodeParams& p, const TmaMaps& maps, uint8_t* base,
-                             uint64_t* bars, volatile int* abort, int seg_lo, int seg_hi, int lane) {
-    TileCursor cur;
-    cur.init(p, seg_lo, seg_hi);
-    if (cur.valid()) cur.prefetch(p, lane, true);
-    const uint32_t sbase = smem_u32(base);
-    int i = 0;
-    for (bool more = cur.valid(); more; ++i) {
-        const int slot = i % kStages;
-        const uint32_t u = static_cast<uint32_t>(i / kStages);
-        int32_t sl[4];
-        cur.rows(p, sl, true);
-        // the next tile's index loads fly while this tile is issued
-        cur.advance(p);
-        more = cur.valid();
-        if (more) cur.prefetch(p, lane, true);
-        if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
-        if (lane == 0) mbar_arrive_expect_tx(&bars[KV_FULL + slot], kTmaBytes);
-        __syncwarp();
-        if (4 * lane < kTT) {                  // lane l gathers rows 4l .. 4l+3
-            int32_t rc[4];
+// Copies warp w's share of tile i into its stage: c_kv block w (8 chunks of
+// 16 B per row, four rows per instruction) and k_pe rows 8g .. 8g+7 for
+// g = w, w+4, w+8, w+12 (4 chunks per row, eight rows per instruction).
+// `sl` holds the slots of rows lane + 32q.
+__device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage, const int32_t (&sl)[4],
+                                           int w, int lane) {
+    const int r4 = lane >> 3, c8 = lane & 7;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) rc[q] = sl[q] >= 0 ? sl[q] : maps.rows;
-            const uint32_t stage = sbase + kOffStage + slot * kStage;
-#pragma unroll
-            for (int cb = 0; cb < kTmaBlocks; ++cb)
-                tma_gather4(stage + cb * kBlk + 4 * lane * 128, &maps.ckv, cb * 128, rc[0], rc[1],
-                            rc[2], rc[3], &bars[KV_FULL + slot]);
-        }
+    for (int j = 0; j < kTT / 4; ++j) {
+        const int row = 4 * j + r4;
+        const int32_t s = __shfl_sync(0xffffffffu, sl[j >> 3], row & 31);
+        const int64_t ss = s >= 0 ? s : 0;
+        cp_async16(stage + w * kBlk + row * 128 + ((c8 ^ (row & 7)) << 4),
+                   p.ckv + ss * p.ckv_stride + w * 128 + c8 * 16, s >= 0 ? 16u : 0u);
     }
-    // copies still in flight (only after an abort) land before the CTA exits
-    volatile int never = 0;
-    for (int j = i - kStages < 0 ? 0 : i - kStages; j < i; ++j)
-        mbar_wait(&bars[KV_FULL + j % kStages], (static_cast<uint32_t>(j / kStages)) & 1, &never,
-                  p.flags, 1000000000ull);
+    const int r8 = lane >> 2, c4 = lane & 3;
+#pragma unroll
+    for (int gq = 0; gq < kTT / 8 / kFillWarps; ++gq) {
+        const int g = w + kFillWarps * gq;
+        const int row = 8 * g + r8;
+        const int32_t s = __shfl_sync(0xffffffffu, sl[g >> 2], row & 31);
+        const int64_t ss = s >= 0 ? s : 0;
+        cp_async16(stage + 4 * kBlk + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4),
+                   p.kpe + ss * p.kpe_stride + c4 * 16, s >= 0 ? 16u : 0u);
+    }
 }
 
-__device__ void producer_lsu(const DecodeParams& p, uint8_t* base, uint64_t* bars,
-                             volatile int* abort, int seg_lo, int seg_hi, int lane) {
+__device__ void scheduler_fill(const DecodeParams& p, uint8_t* base, uint64_t* bars,
+                               volatile int* abort, int seg_lo, int seg_hi, int lane) {
+    int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
+    // one prefetch sweep per row when k_pe follows c_kv in the same row
+    const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
     TileCursor cur;
     cur.init(p, seg_lo, seg_hi);
-    if (cur.valid()) cur.prefetch(p, lane, false);
-    int i = 0;
-    for (bool more = cur.valid(); more; ++i) {
-        const int slot = i % kStages;
-        const uint32_t u = static_cast<uint32_t>(i / kStages);
+    if (cur.valid()) cur.prefetch(p, lane);
+    int n_sched = 0;
+    // publishes the cursor's tile in the ring and prefetches its rows to L2
+    auto schedule = [&]() -> bool {
+        const int e = n_sched % kRing;
+        const uint32_t u = static_cast<uint32_t>(n_sched / kRing);
         int32_t sl[4];
-        cur.rows(p, sl, false);
+        cur.rows(p, sl);
         cur.advance(p);
-        more = cur.valid();
-        if (more) cur.prefetch(p, lane, false);
-        if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
-        uint8_t* stage = base + kOffStage + slot * kStage;
-        // c_kv blocks kTmaBlocks..3: 8 chunks (128 B) per row, four rows per
-        // instruction
-        const int r4 = lane >> 3, c8 = lane & 7;
+        if (cur.valid()) cur.prefetch(p, lane);       // the next tile's index loads fly meanwhile
 #pragma unroll
-        for (int cb = kTmaBlocks; cb < 4; ++cb) {
-#pragma unroll
-            for (int j = 0; j < kTT / 4; ++j) {
-                const int row = 4 * j + r4;
-                const int32_t s = __shfl_sync(0xffffffffu, sl[j >> 3], row & 31);
-                const int64_t ss = s >= 0 ? s : 0;
-                cp_async16(stage + cb * kBlk + row * 128 + ((c8 ^ (row & 7)) << 4),
-                           p.ckv + ss * p.ckv_stride + cb * 128 + c8 * 16, s >= 0 ? 16u : 0u);
+        for (int q = 0; q < 4; ++q) {
+            if (sl[q] < 0) continue;
+            const uint8_t* row = p.ckv + int64_t(sl[q]) * p.ckv_stride;
+            if (joint) {
+                prefetch_row_l2<kDQk>(row);
+            } else {
+                prefetch_row_l2<kDCkv>(row);
+                prefetch_row_l2<kDKpe>(p.kpe + int64_t(sl[q]) * p.kpe_stride);
             }
         }
-        // k_pe: 4 chunks per row, eight rows per instruction (64-byte swizzle)
-        const int r8 = lane >> 2, c4 = lane & 3;
+        if (!mbar_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) return false;
+        *reinterpret_cast<int4*>(ring + e * kTT + 4 * lane) = make_int4(sl[0], sl[1], sl[2], sl[3]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[SL_FULL + e]);
+        ++n_sched;
+        return true;
+    };
+    bool ok = true;
+    while (ok && cur.valid() && n_sched < kAhead) ok = schedule();
+    for (int i = 0; ok; ++i) {
+        if (cur.valid() && !schedule()) break;        // keeps kAhead tiles published ahead
+        if (i >= n_sched) break;
+        const int slot = i % kStages;
+        const uint32_t u = static_cast<uint32_t>(i / kStages);
+        const int e = i % kRing;
+        int32_t sl[4];                                // rows lane + 32 q (own writes: no wait)
 #pragma unroll
-        for (int g = 0; g < kTT / 8; ++g) {
-            const int row = 8 * g + r8;
-            const int32_t s = __shfl_sync(0xffffffffu, sl[g >> 2], row & 31);
-            const int64_t ss = s >= 0 ? s : 0;
-            cp_async16(stage + 4 * kBlk + row * 64 + ((c4 ^ ((row >> 1) & 3)) << 4),
-                       p.kpe + ss * p.kpe_stride + c4 * 16, s >= 0 ? 16u : 0u);
-        }
+        for (int q = 0; q < 4; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
+        if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
+        fill_share(p, base + kOffStage + slot * kStage, sl, 0, lane);
+        mbar_arrive_cp_async(&bars[KV_FULL + slot]);
+    }
+    cp_async_wait<0>();
+}
+
+__device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
+                          int seg_lo, int seg_hi, int w, int lane) {
+    const int32_t* ring = reinterpret_cast<const int32_t*>(base + kOffRing);
+    const int total = count_tiles(p, seg_lo, seg_hi);
+    for (int i = 0; i < total; ++i) {
+        const int slot = i % kStages;
+        const uint32_t u = static_cast<uint32_t>(i / kStages);
+        const int e = i % kRing;
+        if (!mbar_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, abort, p.flags)) break;
+        int32_t sl[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[SL_EMPTY + e]);
+        if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
+        fill_share(p, base + kOffStage + slot * kStage, sl, w, lane);
         mbar_arrive_cp_async(&bars[KV_FULL + slot]);
     }
     cp_async_wait<0>();
@@ -299,44 +316,76 @@ struct MmaCtx {
     uint32_t* flags;
 };
 
+// Descriptors are built once per operand region and advanced by adding the
+// (compile-time) byte offset / 16 to the start-address field: the issuing
+// thread then spends a 64-bit add per MMA instead of rebuilding the word,
+// which on GB300 halves the time a thread takes to issue one MMA.  The field
+// cannot carry: shared addresses stay below 256 KB.
+__device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_offset) {
+    return base_desc + static_cast<uint64_t>(byte_offset >> 4);
+}
+
 __device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
     const int slot = i & 1;
     const uint32_t stage = c.sbase + kOffStage + (i % kStages) * kStage;
     const uint32_t qb = c.sbase + kOffQ + qs * kQBytes;
+    // c_kv channels: 128-byte swizzle, 8-row groups 1 KB apart; k_pe
+    // channels: 64-byte swizzle, 8-row groups 512 B apart
+    const uint64_t a128 = smem_desc(stage, 16, 1024, kSwizzle128B);
+    const uint64_t b128 = smem_desc(qb, 16, 1024, kSwizzle128B);
+    const uint64_t a64 = smem_desc(stage + 4 * kBlk, 16, 512, kSwizzle64B);
+    const uint64_t b64 = smem_desc(qb + 4 * kQBlk, 16, 512, kSwizzle64B);
+    const uint32_t d = c.tmem + kColS + 32 * slot;
 #pragma unroll
     for (int ks = 0; ks < kKSteps; ++ks) {
-        uint64_t a, b;
-        if (ks < 16) {           // c_kv channels: 128-byte swizzle, 8-row groups 1 KB apart
-            a = smem_desc(stage + (ks >> 2) * kBlk + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-            b = smem_desc(qb + (ks >> 2) * kQBlk + (ks & 3) * 32, 16, 1024, kSwizzle128B);
-        } else {                 // k_pe channels: 64-byte swizzle, 8-row groups 512 B apart
-            a = smem_desc(stage + 4 * kBlk + (ks - 16) * 32, 16, 512, kSwizzle64B);
-            b = smem_desc(qb + 4 * kQBlk + (ks - 16) * 32, 16, 512, kSwizzle64B);
-        }
-        mma_e4m3(c.tmem + kColS + 32 * slot, a, b, c.idesc_qk, ks > 0);
+        const uint64_t a = ks < 16 ? desc_at(a128, (ks >> 2) * kBlk + (ks & 3) * 32)
+                                   : desc_at(a64, (ks - 16) * 32);
+        const uint64_t b = ks < 16 ? desc_at(b128, (ks >> 2) * kQBlk + (ks & 3) * 32)
+                                   : desc_at(b64, (ks - 16) * 32);
+        mma_e4m3(d, a, b, c.idesc_qk, ks > 0);
     }
     mma_commit(&c.bars[S_FULL + slot]);
 }
 
-__device__ __forceinline__ void issue_pv(const MmaCtx& c, int j) {
-    const int slot = j & 1;
+// PV of tile j into O buffer `ob`; the segment's first tile overwrites it.
+__device__ __forceinline__ void issue_pv(const MmaCtx& c, int j, int ob, bool first) {
     const int kv = j % kStages;
-    const uint32_t stage = c.sbase + kOffStage + kv * kStage;
-    const uint32_t pb = c.sbase + kOffP + slot * kPBytes;
+    // A = V^T: 128 channels (one column block) x 32 tokens, MN-major;
+    // B = [P1;P2]^T: 32 tokens x 32 (term, head), MN-major, unswizzled
+    const uint64_t a0 = smem_desc(c.sbase + kOffStage + kv * kStage, kBlk, 1024, kSwizzle128B);
+    const uint64_t b0 = smem_desc(c.sbase + kOffP + (j & 1) * kPBytes, 128, kPUnit, kSwizzleNone);
+    const uint32_t d = c.tmem + kColO + 128 * ob;
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-        for (int ks = 0; ks < kTT / 32; ++ks) {
-            // A = V^T: 128 channels (one column block) x 32 tokens, MN-major
-            const uint64_t a = smem_desc(stage + mb * kBlk + ks * 32 * 128, kBlk, 1024, kSwizzle128B);
-            // B = [P1;P2]^T: 32 tokens x 32 (term, head), MN-major, unswizzled
-            const uint64_t b = smem_desc(pb + ks * 32 * 16, 128, kPUnit, kSwizzleNone);
-            mma_e4m3(c.tmem + kColO + 128 * slot + 32 * mb, a, b, c.idesc_pv, ks > 0);
-        }
+        for (int ks = 0; ks < kTT / 32; ++ks)
+            mma_e4m3(d + 32 * mb, desc_at(a0, mb * kBlk + ks * 32 * 128), desc_at(b0, ks * 32 * 16),
+                     c.idesc_pv, ks > 0 || !first);
     }
-    mma_commit(&c.bars[O_FULL + slot]);
+    mma_commit(&c.bars[PV_DONE + (j & 1)]);
     mma_commit(&c.bars[KV_EMPTY + kv]);       // the stage may be refilled
 }
+
+// Position in the CTA's tile sequence: segment ordinal k and tile it of it.
+struct SegWalk {
+    int si, seg_hi, it, k;
+    Seg sg;
+    __device__ void init(const DecodeParams& p, int lo, int hi) {
+        si = lo;
+        seg_hi = hi;
+        it = 0;
+        k = 0;
+        while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
+    }
+    __device__ void advance(const DecodeParams& p) {
+        if (++it == sg.ntiles) {
+            it = 0;
+            ++k;
+            ++si;
+            while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
+        }
+    }
+};
 
 // QK^T of tile i and PV of tile j < i are independent once their inputs are
 // ready; the issuer polls both and sends whichever is ready (PV first, since
@@ -348,22 +397,24 @@ __device__ void mma_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, i
         if (sg.ntiles == 0 && sg.t1 > sg.t0) raise_flag(p.flags, MLA_FLAG_PLAN_MISMATCH);
         total += sg.ntiles;
     }
-    int si = seg_lo, it = 0, k = 0;
-    Seg sg{};
-    while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
+    SegWalk wq, wp;                    // QK and PV positions
+    wq.init(p, seg_lo, seg_hi);
+    wp.init(p, seg_lo, seg_hi);
     int qk = 0, pv = 0;
     uint64_t last = global_ns();
     uint32_t spins = 0;
     while (pv < total) {
         bool did = false;
         if (pv < qk) {
-            const int slot = pv & 1;
             const uint32_t u = static_cast<uint32_t>(pv) >> 1;
-            if (mbar_test(&c.bars[P_FULL + slot], u & 1) &&
-                mbar_test(&c.bars[O_FREE + slot], (u & 1) ^ 1)) {
+            const int ob = wp.k & 1;
+            const uint32_t ou = static_cast<uint32_t>(wp.k) >> 1;
+            if (mbar_test(&c.bars[P_FULL + (pv & 1)], u & 1) &&
+                (wp.it != 0 || mbar_test(&c.bars[O_FREE + ob], (ou & 1) ^ 1))) {
                 fence_after_sync();
                 fence_proxy_async_smem();
-                issue_pv(c, pv);
+                issue_pv(c, pv, ob, wp.it == 0);
+                wp.advance(p);
                 ++pv;
                 did = true;
             }
@@ -371,25 +422,18 @@ __device__ void mma_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, i
         if (!did && qk < total && qk - pv < 2) {
             const int slot = qk & 1;
             const uint32_t u = static_cast<uint32_t>(qk) >> 1;
-            const int qs = k & 1;
-            const uint32_t qu = static_cast<uint32_t>(k) >> 1;
+            const int qs = wq.k & 1;
+            const uint32_t qu = static_cast<uint32_t>(wq.k) >> 1;
             const int kv = qk % kStages;
             const uint32_t kvu = static_cast<uint32_t>(qk / kStages);
-            if ((it != 0 || mbar_test(&c.bars[Q_FULL + qs], qu & 1)) &&
+            if ((wq.it != 0 || mbar_test(&c.bars[Q_FULL + qs], qu & 1)) &&
                 mbar_test(&c.bars[KV_FULL + kv], kvu & 1) &&
                 mbar_test(&c.bars[S_FREE + slot], (u & 1) ^ 1)) {
                 fence_after_sync();
                 fence_proxy_async_smem();
                 issue_qk(c, qk, qs);
-                if (it == sg.ntiles - 1) {
-                    mma_commit(&c.bars[Q_FREE + qs]);     // q buffer of this segment done
-                    it = 0;
-                    ++k;
-                    ++si;
-                    while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
-                } else {
-                    ++it;
-                }
+                if (wq.it == wq.sg.ntiles - 1) mma_commit(&c.bars[Q_FREE + qs]);   // q buffer done
+                wq.advance(p);
                 ++qk;
                 did = true;
             }
@@ -398,7 +442,7 @@ __device__ void mma_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, i
             spins = 0;
             last = global_ns();
         } else {
-            __nanosleep(64);           // leave issue slots to the softmax warp on this SMSP
+            __nanosleep(32);
         }
         if (!did && (++spins & 63) == 0) {
             if (*c.abort) break;
@@ -419,32 +463,41 @@ __device__ void mma_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, i
 
 __device__ void q_prep(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                        int seg_lo, int seg_hi, int head0, int lane) {
-    // lane = (head, half row): head lane/2, 16-channel chunks 18*(lane&1) ..
-    // +17, all loads issued before any is used (one memory latency per
-    // segment instead of one per head)
+    // The request's BF16 q rows arrive in shared memory by bulk copy (one
+    // memory latency per segment); then lane = (head, half row): head
+    // lane/2, 16-channel chunks 18*(lane&1) .. +17 are scaled and split.
     constexpr int kChunks = kDQk / 16 / 2;          // 18 chunks of 16 channels per lane
     float* coefs = reinterpret_cast<float*>(base + kOffCoef);
+    const uint8_t* raw = base + kOffQRaw;
     const int r = lane >> 1, c0 = (lane & 1) * kChunks;
-    const int head = head0 + r;
-    const bool valid = head < p.heads;
+    const int nh = p.heads - head0 < kHeadsPerCta ? p.heads - head0 : kHeadsPerCta;
+    const bool valid = r < nh;
+    const uint4* src = reinterpret_cast<const uint4*>(raw + r * kQRawRow + 32 * c0);
     int k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k & 1;
         const uint32_t qu = static_cast<uint32_t>(k) >> 1;
-        const uint4* src = reinterpret_cast<const uint4*>(
-            p.q + int64_t(sg.b) * p.q_sb + int64_t(valid ? head : 0) * p.q_sh + 16 * c0);
-        // pass 1: the head's largest magnitude (9 chunks in flight at a time)
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&bars[Q_RAW], static_cast<uint32_t>(nh * kDQk * 2));
+            for (int h = 0; h < nh; ++h)
+                bulk_copy_g2s(smem_u32(raw + h * kQRawRow),
+                              p.q + int64_t(sg.b) * p.q_sb + int64_t(head0 + h) * p.q_sh, kDQk * 2,
+                              &bars[Q_RAW]);
+        }
+        if (!mbar_wait(&bars[Q_RAW], static_cast<uint32_t>(k) & 1, abort, p.flags)) {
+            // the copy lands before the CTA may exit
+            volatile int never = 0;
+            mbar_wait(&bars[Q_RAW], static_cast<uint32_t>(k) & 1, &never, p.flags, 1000000000ull);
+            break;
+        }
         float amax = 0.f;
-#pragma unroll
-        for (int g = 0; g < 2; ++g) {
-            uint4 v[kChunks];
-#pragma unroll
-            for (int j = 0; j < kChunks; ++j) v[j] = valid ? src[g * kChunks + j] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int j = 0; j < kChunks; ++j) {
-                const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        if (valid) {
+#pragma unroll 6
+            for (int j = 0; j < 2 * kChunks; ++j) {
+                const uint4 v = src[j];
+                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
@@ -459,8 +512,8 @@ __device__ void q_prep(const DecodeParams& p, uint8_t* base, uint64_t* bars, vol
         const float scale = ldexpf(1.f, sigma);
         if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
         uint8_t* qb = base + kOffQ + qs * kQBytes;
-        // pass 2 (re-read, now cached): split each value into two E4M3 terms
-#pragma unroll 1
+        // split each value into two E4M3 terms
+#pragma unroll 2
         for (int cc16 = 0; cc16 < kChunks; ++cc16) {
             const uint4 va = valid ? src[2 * cc16] : make_uint4(0, 0, 0, 0);
             const uint4 vb = valid ? src[2 * cc16 + 1] : make_uint4(0, 0, 0, 0);
@@ -501,6 +554,8 @@ __device__ void q_prep(const DecodeParams& p, uint8_t* base, uint64_t* bars, vol
         if ((lane & 1) == 0)
             coefs[qs * kHeadsPerCta + r] =
                 valid ? ldexpf(p.softmax_scale * p.k_scale * kLog2e, -sigma) : 0.f;
+        // the raw rows may be overwritten by the next segment's copy and the
+        // split terms are read by the tensor core: both are async-proxy uses
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[Q_FULL + qs]);
@@ -508,7 +563,7 @@ __device__ void q_prep(const DecodeParams& p, uint8_t* base, uint64_t* bars, vol
     }
 }
 
-// ------------------------------------------------- softmax / correction WG
+// ------------------------------------------------- softmax / rescale WG
 
 struct WgCtx {
     uint8_t* base;
@@ -516,28 +571,28 @@ struct WgCtx {
     uint32_t tmem_lane;     // TMEM base + this warp's lane quadrant
     volatile int* abort;
     uint32_t* flags;
-    int t, wq, lane;        // thread 0..127, warp 0..3, lane
+    int row;                // TMEM lane = token of a tile / channel of a block
+    int wq, lane;           // softmax warp 0..3, lane
 };
 
-__device__ __forceinline__ bool correction(const WgCtx& w, int j, const float (&alpha)[16],
-                                           float (&o)[4][16]) {
-    const int slot = j & 1;
-    const uint32_t u = static_cast<uint32_t>(j) >> 1;
-    if (!mbar_wait(&w.bars[O_FULL + slot], u & 1, w.abort, w.flags)) return false;
-    fence_after_sync();
+// O (one segment's accumulator) *= alpha per head, in TMEM.  Columns h and
+// 16 + h of each 128-channel block hold head h's two P terms.
+__device__ __forceinline__ void rescale_o(const WgCtx& w, uint32_t ocol, const float (&alpha)[16]) {
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
         uint32_t r1[16], r2[16];
-        tmem_ld16(w.tmem_lane + kColO + 128 * slot + 32 * mb, r1);
-        tmem_ld16(w.tmem_lane + kColO + 128 * slot + 32 * mb + 16, r2);
+        tmem_ld16(w.tmem_lane + ocol + 32 * mb, r1);
+        tmem_ld16(w.tmem_lane + ocol + 32 * mb + 16, r2);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 16; ++h)
-            o[mb][h] = fmaf(o[mb][h], alpha[h], __uint_as_float(r1[h]) + __uint_as_float(r2[h]));
+        for (int h = 0; h < 16; ++h) {
+            r1[h] = __float_as_uint(__uint_as_float(r1[h]) * alpha[h]);
+            r2[h] = __float_as_uint(__uint_as_float(r2[h]) * alpha[h]);
+        }
+        tmem_st16(w.tmem_lane + ocol + 32 * mb, r1);
+        tmem_st16(w.tmem_lane + ocol + 32 * mb + 16, r2);
     }
-    fence_before_sync();
-    mbar_arrive(&w.bars[O_FREE + slot]);
-    return true;
+    tmem_wait_st();
 }
 
 // Maximum over the 32 lanes of 16 values at once by halving exchanges
@@ -564,32 +619,35 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
     int* vote = reinterpret_cast<int*>(w.base + kOffFlag);
     const float* coefs = reinterpret_cast<const float*>(w.base + kOffCoef);
     uint8_t* pbase = w.base + kOffP;
+    const int32_t* ring = reinterpret_cast<const int32_t*>(w.base + kOffRing);
     int i = 0, k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k & 1;
         const uint32_t qu = static_cast<uint32_t>(k) >> 1;
+        const uint32_t ocol = kColO + 128 * (k & 1);
         if (!mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags)) return;
-        float coef[16];
-#pragma unroll
-        for (int h = 0; h < 16; ++h) coef[h] = coefs[qs * kHeadsPerCta + h];
-        mbar_arrive(&w.bars[Q_FREE + qs]);
-        const int32_t* pages = p.indices + p.indptr[sg.b];
+        // the segment's score multipliers stay in shared memory (q buffer qs
+        // is released at the end of the segment)
+        const float* coef = coefs + qs * kHeadsPerCta;
 
-        float m[16], l[16], alpha_pend[16], o[4][16];
+        float m[16], l[16];
 #pragma unroll
         for (int h = 0; h < 16; ++h) {
             m[h] = -INFINITY;
             l[h] = 0.f;
-            alpha_pend[h] = 0.f;
-#pragma unroll
-            for (int mb = 0; mb < 4; ++mb) o[mb][h] = 0.f;
         }
         for (int it = 0; it < sg.ntiles; ++it, ++i) {
             const int slot = i & 1;
             const uint32_t u = static_cast<uint32_t>(i) >> 1;
-            const bool valid = token_slot(p, pages, sg.t0 + it * kTT + w.t, sg.t1, false) >= 0;
+            // row validity from the scheduler's slot list (a -1 row is zero-filled)
+            const int e = i % kRing;
+            if (!mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, w.abort, w.flags))
+                return;
+            const bool valid = ring[e * kTT + w.row] >= 0;
+            __syncwarp();
+            if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
             if (!mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags)) return;
             fence_after_sync();
             uint32_t r1[16], r2[16];
@@ -613,56 +671,61 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             if (w.lane == 0) vb[w.wq] = need;
             wg_bar();
             need = vb[0] | vb[1] | vb[2] | vb[3];
-            float alpha[16];
             if (need) {
                 const float wmax = warp_max16(s, w.lane);
                 float* rb = red + (i & 1) * 64;
                 if ((w.lane & 1) == 0) rb[w.wq * 16 + (w.lane >> 1)] = wmax;
                 wg_bar();
+                float alpha[16];
 #pragma unroll
                 for (int h = 0; h < 16; ++h) {
                     const float tmax = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
                     const float mn = fmaxf(m[h], tmax);
-                    alpha[h] = mn == -INFINITY ? 1.f : fast_exp2(m[h] - mn);
+                    alpha[h] = m[h] == -INFINITY ? 0.f : fast_exp2(m[h] - mn);
                     m[h] = mn;
+                    l[h] *= alpha[h];
                 }
-            } else {
-#pragma unroll
-                for (int h = 0; h < 16; ++h) alpha[h] = 1.f;
+                if (it > 0) {
+                    // O holds tiles up to i - 1: rescale once PV(i - 1) has landed
+                    const int j = i - 1;
+                    if (!mbar_wait(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort,
+                                   w.flags))
+                        return;
+                    fence_after_sync();
+                    rescale_o(w, ocol, alpha);
+                }
             }
-            // P = 2^(s - m) <= 2^kTau, stored as two E4M3 terms of p * kPScale
+            // P = 2^(s - m) <= 2^kTau, stored as two E4M3 terms of p * kPScale;
+            // its buffer was last read by PV(i - 2)
+            if (i >= 2 && !mbar_wait(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags)) return;
             uint32_t pk1[4], pk2[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
+            for (int e4 = 0; e4 < 4; ++e4) {
                 uint32_t w1 = 0, w2 = 0;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int h = 4 * e + 2 * hh;
+                    const int h = 4 * e4 + 2 * hh;
                     const float x0 = m[h] == -INFINITY ? 0.f : fast_exp2(s[h] - m[h]) * kPScale;
                     const float x1 = m[h + 1] == -INFINITY ? 0.f : fast_exp2(s[h + 1] - m[h + 1]) * kPScale;
                     const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
                     const float2 d1 = e4m3x2_to_float2(b1);
                     const uint16_t b2 = f32x2_to_e4m3x2(x0 - d1.x, x1 - d1.y);
                     const float2 d2 = e4m3x2_to_float2(b2);
-                    l[h] = fmaf(l[h], alpha[h], d1.x + d2.x);
-                    l[h + 1] = fmaf(l[h + 1], alpha[h + 1], d1.y + d2.y);
+                    l[h] += d1.x + d2.x;
+                    l[h + 1] += d1.y + d2.y;
                     w1 |= static_cast<uint32_t>(b1) << (16 * hh);
                     w2 |= static_cast<uint32_t>(b2) << (16 * hh);
                 }
-                pk1[e] = w1;
-                pk2[e] = w2;
+                pk1[e4] = w1;
+                pk2[e4] = w2;
             }
-            uint8_t* pb = pbase + slot * kPBytes + w.t * 16;
+            uint8_t* pb = pbase + slot * kPBytes + w.row * 16;
             *reinterpret_cast<uint4*>(pb) = make_uint4(pk1[0], pk1[1], pk1[2], pk1[3]);
             *reinterpret_cast<uint4*>(pb + kPUnit) = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
             fence_proxy_async_smem();
+            fence_before_sync();                    // orders a rescale's TMEM stores too
             mbar_arrive(&w.bars[P_FULL + slot]);
-
-            if (it > 0 && !correction(w, i - 1, alpha_pend, o)) return;
-#pragma unroll
-            for (int h = 0; h < 16; ++h) alpha_pend[h] = alpha[h];
         }
-        if (!correction(w, i - 1, alpha_pend, o)) return;
 
         // ---- epilogue: denominators over the token lanes, normalise, store
 #pragma unroll
@@ -675,51 +738,57 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             for (int h = 0; h < 16; ++h) lsum[w.wq * 16 + h] = l[h];
         }
         wg_bar();
-        float L[16];
+        float inv[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) L[h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
+        for (int h = 0; h < 16; ++h) l[h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
         wg_bar();                                   // lsum is reused by the next segment
+#pragma unroll
+        for (int h = 0; h < 16; ++h) inv[h] = l[h] > 0.f ? p.k_scale / l[h] : 0.f;
+        const int jl = i - 1;                       // the segment's last tile
+        if (!mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags))
+            return;
+        fence_after_sync();
         const int H = p.heads;
-        // o and L are both in units of p * kPScale; lse = m + log2(sum p)
+        // o and l are both in units of p * kPScale; lse = m + log2(sum p)
         const float lse_off = -kTau;                 // kPScale = 2^kTau
-        if (sg.part < 0) {
-            uint16_t* out = p.out + (int64_t(sg.b) * H + head0) * kDCkv + w.t;
+#pragma unroll 1
+        for (int mb = 0; mb < 4; ++mb) {
+            uint32_t r1[16], r2[16];
+            tmem_ld16(w.tmem_lane + ocol + 32 * mb, r1);
+            tmem_ld16(w.tmem_lane + ocol + 32 * mb + 16, r2);
+            tmem_wait_ld();
+            const int ch = mb * 128 + w.row;
+            if (sg.part < 0) {
+                uint16_t* out = p.out + (int64_t(sg.b) * H + head0) * kDCkv + ch;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                if (head0 + h >= H) break;
-                const float inv = L[h] > 0.f ? p.k_scale / L[h] : 0.f;
+                for (int h = 0; h < 16; ++h) {
+                    if (head0 + h >= H) break;
+                    const float o = __uint_as_float(r1[h]) + __uint_as_float(r2[h]);
+                    out[h * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o * inv[h]));
+                }
+            } else {
+                float* po = p.part_o + (int64_t(sg.part) * H + head0) * kDCkv + ch;
 #pragma unroll
-                for (int mb = 0; mb < 4; ++mb)
-                    out[h * kDCkv + mb * 128] = __bfloat16_as_ushort(__float2bfloat16_rn(o[mb][h] * inv));
+                for (int h = 0; h < 16; ++h) {
+                    if (head0 + h >= H) break;
+                    po[h * kDCkv] = (__uint_as_float(r1[h]) + __uint_as_float(r2[h])) * inv[h];
+                }
             }
-            if (w.t == 0) {
+        }
+        fence_before_sync();
+        mbar_arrive(&w.bars[O_FREE + (k & 1)]);      // the next segment but one may overwrite O
+        mbar_arrive(&w.bars[Q_FREE + qs]);
+        if (w.row == 0) {
+            float* dst = sg.part < 0 ? p.lse + int64_t(sg.b) * H : p.part_lse + int64_t(sg.part) * H;
 #pragma unroll
-                for (int h = 0; h < 16; ++h)
-                    if (head0 + h < H)
-                        p.lse[int64_t(sg.b) * H + head0 + h] = (m[h] + log2f(L[h]) + lse_off) * kLn2;
-            }
-        } else {
-            float* po = p.part_o + (int64_t(sg.part) * H + head0) * kDCkv + w.t;
-#pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                if (head0 + h >= H) break;
-                const float inv = L[h] > 0.f ? p.k_scale / L[h] : 0.f;
-#pragma unroll
-                for (int mb = 0; mb < 4; ++mb) po[h * kDCkv + mb * 128] = o[mb][h] * inv;
-            }
-            if (w.t == 0) {
-#pragma unroll
-                for (int h = 0; h < 16; ++h)
-                    if (head0 + h < H)
-                        p.part_lse[int64_t(sg.part) * H + head0 + h] = (m[h] + log2f(L[h]) + lse_off) * kLn2;
-            }
+            for (int h = 0; h < 16; ++h)
+                if (head0 + h < H) dst[head0 + h] = (m[h] + log2f(l[h]) + lse_off) * kLn2;
         }
         ++k;
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps) {
+__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBar);
@@ -728,14 +797,19 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        // KV_FULL: 1 TMA arrive (+ transaction bytes) and 32 cp.async arrivals
-        const uint32_t counts[NUM_BARS] = {33, 33, 1, 1, 1, 1, 128, 128, 128, 128,
-                                           1, 1, 128, 128, 1, 1, 129, 129, 1};
-        for (int b = 0; b < NUM_BARS; ++b) mbar_init(&bars[b], counts[b]);
+        // KV_FULL: 32 cp.async arrivals from each fill warp; SL_EMPTY: fill
+        // warps 1-3 and the four softmax warps
+        const uint32_t counts[SL_FULL] = {32 * kFillWarps, 32 * kFillWarps, 1, 1, 1, 1, 128, 128,
+                                          128, 128, 1, 1, 128, 128, 1, 1, 129, 129, 1, 1};
+        for (int b = 0; b < SL_FULL; ++b) mbar_init(&bars[b], counts[b]);
+        for (int e = 0; e < kRing; ++e) {
+            mbar_init(&bars[SL_FULL + e], 1);
+            mbar_init(&bars[SL_EMPTY + e], (kFillWarps - 1) + 4);
+        }
         *abort = 0;
         mbar_fence_init();
     }
-    if (warp == 2) tmem_alloc(tmem_slot, kTmemCols);
+    if (warp == kWarpMma) tmem_alloc(tmem_slot, kTmemCols);
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -744,10 +818,10 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps)
     const int head0 = 0;                          // this kernel serves H <= 16
 
     if (warp == 0) {
-        producer_tma(p, maps, base, bars, abort, seg_lo, seg_hi, lane);
-    } else if (warp == 1) {
-        producer_lsu(p, base, bars, abort, seg_lo, seg_hi, lane);
-    } else if (warp == 2) {
+        scheduler_fill(p, base, bars, abort, seg_lo, seg_hi, lane);
+    } else if (warp < kFillWarps) {
+        fill_warp(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
+    } else if (warp == kWarpMma) {
         if (lane == 0) {
             MmaCtx c;
             c.sbase = smem_u32(base);
@@ -760,61 +834,29 @@ mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TmaMaps maps)
             mma_issuer(p, c, seg_lo, seg_hi);
         }
         __syncwarp();
-    } else if (warp == 3) {
+    } else if (warp == kWarpQ) {
         q_prep(p, base, bars, abort, seg_lo, seg_hi, head0, lane);
     } else {
         WgCtx w;
         w.base = base;
         w.bars = bars;
-        w.wq = warp - 4;
-        w.tmem_lane = tmem + (static_cast<uint32_t>(w.wq * 32) << 16);
+        const int quad = warp & 3;                // a warp reaches TMEM lanes 32 (warp % 4) .. + 31
+        w.tmem_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
         w.abort = abort;
         w.flags = p.flags;
-        w.t = tid - 128;
+        w.row = quad * 32 + lane;
+        w.wq = warp - kWarpWg;
         w.lane = lane;
         softmax_wg(p, w, seg_lo, seg_hi, head0);
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
-    if (warp == 2) tmem_dealloc(tmem, kTmemCols);
+    if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 std::mutex g_mu;
 std::vector<char> g_attr;     // per device: max dynamic smem set
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            f = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
-
-// Row-gather tensor map over a pool: `width` E4M3 channels per row, rows
-// `stride` bytes apart, boxes of one row.
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t stride,
-                 uint32_t box, CUtensorMapSwizzle swz) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {width, rows};
-    const cuuint64_t strides[1] = {stride};
-    const cuuint32_t boxd[2] = {box, 1};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, boxd, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 }  // namespace
 
@@ -832,15 +874,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
             g_attr[dev] = 1;
         }
     }
-    TmaMaps maps;
-    // an empty pool still gets a one-row map: every token is then out of
-    // range, gets row coordinate `rows` and reads zeros
-    if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;   // TMA row coordinates are int32
-    const uint64_t rows = p.num_slots > 0 ? static_cast<uint64_t>(p.num_slots) : 1;
-    maps.rows = static_cast<int32_t>(rows);
-    if (!encode_rows(&maps.ckv, p.ckv, kDCkv, rows, p.ckv_stride, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
+    // slots are held as int32 in the kernel's shared slot lists
+    if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
+    mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -92,6 +92,17 @@ MLA_DEVINLINE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 }
 MLA_DEVINLINE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
+// 32 lanes x 16 columns: thread t writes lane (base + t).
+MLA_DEVINLINE void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+           "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+           "r"(r[15])
+        : "memory");
+}
+MLA_DEVINLINE void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 MLA_DEVINLINE void mbar_init(uint64_t* bar, uint32_t count) {
@@ -139,6 +150,27 @@ MLA_DEVINLINE void tma_gather4(uint32_t dst, const void* tensor_map, int32_t x, 
         :: "r"(dst), "l"(tensor_map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
            "r"(smem_u32(bar))
         : "memory");
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from 16-byte aligned global memory
+// to 16-byte aligned shared memory; completes as transaction bytes on `bar`.
+MLA_DEVINLINE void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+        :: "r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// Has L2 fetch every 128-byte line of the `kBytes` bytes at `row` (one
+// prefetch per line, issued by the calling thread; nothing waits for them).
+template <int kBytes>
+MLA_DEVINLINE void prefetch_row_l2(const void* row) {
+    const char* r = static_cast<const char*>(row);
+#pragma unroll
+    for (int o = 0; o < kBytes; o += 128)
+        asm volatile("prefetch.global.L2 [%0];\n" :: "l"(r + o));
+    // the line of the row's last byte (beyond the loop's lines when the row
+    // starts past the middle of a line)
+    asm volatile("prefetch.global.L2 [%0];\n" :: "l"(r + kBytes - 1));
 }
 
 MLA_DEVINLINE uint64_t global_ns() {
