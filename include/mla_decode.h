@@ -93,7 +93,9 @@ typedef struct mla_plan* mla_plan_t;
  *                   kv_indices[kv_indptr[b] + t / page_size] * page_size
  *                   + t % page_size.
  *  kv_dtype         element type of the pools run() will read.
- *  workspace_bytes  out: device scratch run() needs (split-KV partials).
+ *  workspace_bytes  out: device scratch run() needs: the split-KV partials
+ *                   and, on the tensor-core FP8 path (H <= 16), one
+ *                   18,496-byte image of each request's split query.
  *  stream           the plan's device metadata is uploaded on this stream
  *                   (stream-ordered before later runs on it).
  * Errors: MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED before any allocation;
@@ -131,6 +133,11 @@ mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indptr_host,
  *  workspace        device scratch of at least the planned workspace_bytes,
  *                   256-byte aligned; its contents are not preserved.
  * No host synchronisation, allocation or host<->device copy happens here.
+ * The call enqueues up to three kernels on `stream` (query split, decode,
+ * split-KV merge); on the tensor-core path the decode kernel is launched as a
+ * programmatic dependent of the query split, so it may start early and waits
+ * on the device for the split's results.  Work enqueued before the call is
+ * complete before any of them reads it.
  * Errors: MLA_ERR_INVALID_ARG (NULL / misaligned / plan mismatch),
  * MLA_ERR_WORKSPACE, MLA_ERR_CUDA (launch failure).
  */
@@ -153,7 +160,8 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q_stride_b,
  * framework that owns every GPU allocation, a real-time loop that must not
  * pay cudaMalloc's implicit device synchronisation, code that must not touch
  * the allocator between steps.  This call takes the same arguments as
- * mla_decode_run minus the workspace and keeps the split-KV partials in a
+ * mla_decode_run minus the workspace and keeps its scratch (split-KV
+ * partials, query images) in a
  * fixed array of MLA_STATIC_SCRATCH_BYTES compiled into the library; the
  * call allocates nothing (the plan is built beforehand by mla_decode_plan).
  *  - The array exists once per GPU that loads the library and stays

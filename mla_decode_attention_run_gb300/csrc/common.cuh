@@ -109,6 +109,14 @@ MLA_DEVINLINE float fast_exp2(float x) {
     return y;
 }
 
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start before its predecessor in the stream finishes;
+// griddep_wait() blocks the calling thread until the predecessor grid has
+// completed and its writes are visible, and griddep_launch_dependents() lets
+// the next such kernel start once every block of this grid has called it.
+MLA_DEVINLINE void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+MLA_DEVINLINE void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
 MLA_DEVINLINE void raise_flag(uint32_t* flags, uint32_t bit) {
     if (flags) atomicOr(flags, bit);
 }

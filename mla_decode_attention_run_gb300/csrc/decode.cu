@@ -517,6 +517,8 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
     p.cta_ptr = plan->dev_meta + plan->off_cta;
     p.segs = plan->dev_meta + plan->off_segs;
     p.flags = device_flags_ptr();
+    p.qimg = static_cast<uint8_t*>(workspace) + s.qimg_offset;
+    p.batch = s.batch;
 
     if (s.kernel == DecodeKernel::kTc && num_pool_slots >= INT32_MAX) return MLA_ERR_UNSUPPORTED;
     if (s.num_ctas > 0 && s.kernel == DecodeKernel::kTc) {

@@ -26,9 +26,12 @@ struct DecodeParams {
     const int32_t* cta_ptr;     // plan: segments of CTA c are [cta_ptr[c], cta_ptr[c+1])
     const int32_t* segs;        // plan: 4 ints per segment: request, t0, t1, partial (-1 final)
     uint32_t* flags;            // library flag word
+    uint8_t* qimg;              // tcgen05 path: per-request q images (workspace)
+    int32_t batch;
 };
 
-// Launches the tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` CTAs.
+// Launches the q split kernel and then, as its programmatic dependent, the
+// tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` CTAs.
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream);
 
 }  // namespace mla

@@ -46,8 +46,9 @@
 //   warp 4     one thread issues every tcgen05.mma and commit, polling so
 //              that PV of one tile and QK^T of the next go out in whichever
 //              order their inputs become ready;
-//   warp 5     prepares [q1;q2] and the per-head score multipliers for each
-//              segment (double-buffered; lane = half a head row);
+//   warp 5     fetches each segment's [q1;q2] image and per-head score
+//              multipliers, written by the q split kernel that precedes this
+//              one (double-buffered);
 //   warps 6-9  one thread per TMEM lane: online softmax of a token's 16
 //              heads and the E4M3 split of P, rescaling O when the maximum
 //              moves, and the epilogue (lane = output channel).
@@ -89,7 +90,7 @@ constexpr float kPScale = 16.f;             // P is stored as p * 2^kTau
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kRing = 8;                    // scheduled tiles' slot lists in flight
-constexpr int kAhead = 2;                   // tiles scheduled (and prefetched) beyond the one filling
+constexpr int kAhead = 3;                   // tiles published (and prefetched) beyond the one filling
 static_assert(kAhead + kStages < kRing, "the scheduler may not lap the softmax warps");
 
 // shared memory map (offsets from a 1024-byte aligned base)
@@ -97,12 +98,10 @@ constexpr int kOffStage = 0;
 constexpr int kOffQ = kOffStage + kStages * kStage;
 constexpr int kOffP = kOffQ + 2 * kQBytes;
 constexpr int kOffRing = kOffP + 2 * kPBytes;   // kRing x 128 slots (int32)
-constexpr int kOffQRaw = kOffRing + kRing * kTT * 4;   // BF16 q rows of one request
-constexpr int kQRawRow = kDQk * 2 + 16;   // padded: consecutive heads start 4 banks apart
-constexpr int kOffBar = kOffQRaw + kHeadsPerCta * kQRawRow;
+constexpr int kOffBar = kOffRing + kRing * kTT * 4;
 constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x 16
 constexpr int kOffLsum = kOffRed + 512;     // softmax denominators: 4 warps x 16
-constexpr int kOffCoef = kOffLsum + 256;    // score multipliers: 2 x 16
+constexpr int kOffCoef = kOffLsum + 256;    // score multipliers: 2 x 16 (bulk-copy target)
 constexpr int kOffFlag = kOffCoef + 128;    // rescale votes: 2 x 4 warps
 constexpr int kOffMisc = kOffFlag + 32;     // TMEM base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
@@ -115,10 +114,10 @@ static_assert(kThreads == 32 * (kWarpWg + 4), "four softmax warps after the othe
 enum : int {
     KV_FULL = 0, KV_EMPTY = kStages, S_FULL = 2 * kStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
     PV_DONE = P_FULL + 2, O_FREE = PV_DONE + 2, Q_FULL = O_FREE + 2, Q_FREE = Q_FULL + 2,
-    DONE = Q_FREE + 2, Q_RAW = DONE + 1, SL_FULL = Q_RAW + 1, SL_EMPTY = SL_FULL + kRing,
+    DONE = Q_FREE + 2, SL_FULL = DONE + 1, SL_EMPTY = SL_FULL + kRing,
     NUM_BARS = SL_EMPTY + kRing
 };
-static_assert(NUM_BARS == 36 && NUM_BARS * 8 <= 512, "barrier count table below assumes two stages");
+static_assert(NUM_BARS == 35 && NUM_BARS * 8 <= 512, "barrier count table below assumes two stages");
 
 struct Seg {
     int32_t b, t0, t1, part, ntiles;
@@ -268,11 +267,10 @@ __device__ void scheduler_fill(const DecodeParams& p, uint8_t* base, uint64_t* b
         ++n_sched;
         return true;
     };
-    bool ok = true;
-    while (ok && cur.valid() && n_sched < kAhead) ok = schedule();
-    for (int i = 0; ok; ++i) {
-        if (cur.valid() && !schedule()) break;        // keeps kAhead tiles published ahead
-        if (i >= n_sched) break;
+    // tile 0 is filled as soon as it is resolved; from tile 1 on, tiles up
+    // to i + kAhead are published once tile i's fill is under way
+    bool ok = !cur.valid() || schedule();
+    for (int i = 0; ok && i < n_sched; ++i) {
         const int slot = i % kStages;
         const uint32_t u = static_cast<uint32_t>(i / kStages);
         const int e = i % kRing;
@@ -282,6 +280,8 @@ __device__ void scheduler_fill(const DecodeParams& p, uint8_t* base, uint64_t* b
         if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
         fill_share(p, base + kOffStage + slot * kStage, sl, 0, lane);
         mbar_arrive_cp_async(&bars[KV_FULL + slot]);
+        const int target = i == 0 ? 1 : i + kAhead;
+        while (ok && cur.valid() && n_sched <= target) ok = schedule();
     }
     cp_async_wait<0>();
 }
@@ -460,107 +460,114 @@ __device__ void mma_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, i
 }
 
 // ---------------------------------------------------------------- q prep
+//
+// q is split once per request by a small kernel that runs just before the
+// decode kernel: it writes [q1;q2] as the exact shared-memory image the QK^T
+// MMA reads (128-byte swizzle for the 512 c_kv channels, 64-byte for the 64
+// k_pe channels) plus the per-head score multipliers.  A decode CTA then
+// fetches a segment's q with two bulk copies.
 
-__device__ void q_prep(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                       int seg_lo, int seg_hi, int head0, int lane) {
-    // The request's BF16 q rows arrive in shared memory by bulk copy (one
-    // memory latency per segment); then lane = (head, half row): head
-    // lane/2, 16-channel chunks 18*(lane&1) .. +17 are scaled and split.
-    constexpr int kChunks = kDQk / 16 / 2;          // 18 chunks of 16 channels per lane
-    float* coefs = reinterpret_cast<float*>(base + kOffCoef);
-    const uint8_t* raw = base + kOffQRaw;
-    const int r = lane >> 1, c0 = (lane & 1) * kChunks;
-    const int nh = p.heads - head0 < kHeadsPerCta ? p.heads - head0 : kHeadsPerCta;
-    const bool valid = r < nh;
-    const uint4* src = reinterpret_cast<const uint4*>(raw + r * kQRawRow + 32 * c0);
+// Splits 16 BF16 values (two uint4) scaled by `scale` into two E4M3 terms.
+__device__ __forceinline__ void split_chunk(const uint4& va, const uint4& vb, float scale, uint4& t1,
+                                            uint4& t2) {
+    const uint32_t w8[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+    uint32_t o1[4], o2[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        uint32_t lo1 = 0, lo2 = 0;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint32_t w = w8[2 * e + hh];
+            const float x0 = __uint_as_float(w << 16) * scale;
+            const float x1 = __uint_as_float(w & 0xffff0000u) * scale;
+            const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
+            const float2 d = e4m3x2_to_float2(b1);
+            const uint16_t b2 = f32x2_to_e4m3x2(x0 - d.x, x1 - d.y);
+            lo1 |= static_cast<uint32_t>(b1) << (16 * hh);
+            lo2 |= static_cast<uint32_t>(b2) << (16 * hh);
+        }
+        o1[e] = lo1;
+        o2[e] = lo2;
+    }
+    t1 = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    t2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+}
+
+__device__ __forceinline__ float amax_bf16x8(const uint4& v, float a) {
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        a = fmaxf(a, fmaxf(fabsf(__uint_as_float(w4[e] << 16)), fabsf(__uint_as_float(w4[e] & 0xffff0000u))));
+    return a;
+}
+
+constexpr int kSplitThreads = 64;
+
+// One warp per (request, head row): lane c splits 16-channel chunk c of c_kv,
+// lanes 0-3 also chunk c of k_pe.  Heads >= H get zero rows and multiplier 0.
+__global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const DecodeParams p) {
+    griddep_launch_dependents();                // the decode kernel may start loading KV now
+    const int wg = (blockIdx.x * kSplitThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int b = wg / kHeadsPerCta, r = wg % kHeadsPerCta;
+    if (b >= p.batch) return;
+    const bool valid = r < p.heads;
+    const uint4* src = reinterpret_cast<const uint4*>(p.q + int64_t(b) * p.q_sb + int64_t(valid ? r : 0) * p.q_sh);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    const uint4 va = valid ? src[2 * lane] : z, vb = valid ? src[2 * lane + 1] : z;
+    const bool rope = lane < 4;
+    const uint4 ra = valid && rope ? src[64 + 2 * lane] : z, rb = valid && rope ? src[64 + 2 * lane + 1] : z;
+    float amax = amax_bf16x8(rb, amax_bf16x8(ra, amax_bf16x8(vb, amax_bf16x8(va, 0.f))));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e2 = 0;
+    frexpf(amax, &e2);                              // amax = m * 2^e2, m in [0.5, 1)
+    int sigma = amax > 0.f ? 8 - e2 : 0;            // max |q| * 2^sigma in [128, 256)
+    sigma = sigma > 100 ? 100 : (sigma < -100 ? -100 : sigma);
+    const float scale = ldexpf(1.f, sigma);
+    uint8_t* img = p.qimg + int64_t(b) * kTcQImageBytes;
+    const int row1 = r, row2 = kHeadsPerCta + r;
+    uint4 t1, t2;
+    split_chunk(va, vb, scale, t1, t2);
+    {                                               // c_kv: 128-byte rows, 128-byte swizzle
+        const int cb = lane >> 3, cc = lane & 7;
+        *reinterpret_cast<uint4*>(img + cb * kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4)) = t1;
+        *reinterpret_cast<uint4*>(img + cb * kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4)) = t2;
+    }
+    if (rope) {                                     // k_pe: 64-byte rows, 64-byte swizzle
+        split_chunk(ra, rb, scale, t1, t2);
+        *reinterpret_cast<uint4*>(img + 4 * kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4)) = t1;
+        *reinterpret_cast<uint4*>(img + 4 * kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4)) = t2;
+    }
+    if (lane == 0)
+        reinterpret_cast<float*>(img + kQBytes)[r] =
+            valid ? ldexpf(p.softmax_scale * p.k_scale * kLog2e, -sigma) : 0.f;
+}
+static_assert(kTcQImageBytes == kQBytes + kHeadsPerCta * 4, "q image = smem q buffer + multipliers");
+
+// Warp 5: fetches each segment's q image into q buffer k & 1 (and its
+// multipliers) once the split kernel has finished.
+__device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
+                        int seg_lo, int seg_hi, int lane) {
+    if (lane != 0) return;
+    griddep_wait();                                 // the q images are complete
     int k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k & 1;
         const uint32_t qu = static_cast<uint32_t>(k) >> 1;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars[Q_RAW], static_cast<uint32_t>(nh * kDQk * 2));
-            for (int h = 0; h < nh; ++h)
-                bulk_copy_g2s(smem_u32(raw + h * kQRawRow),
-                              p.q + int64_t(sg.b) * p.q_sb + int64_t(head0 + h) * p.q_sh, kDQk * 2,
-                              &bars[Q_RAW]);
-        }
-        if (!mbar_wait(&bars[Q_RAW], static_cast<uint32_t>(k) & 1, abort, p.flags)) {
-            // the copy lands before the CTA may exit
-            volatile int never = 0;
-            mbar_wait(&bars[Q_RAW], static_cast<uint32_t>(k) & 1, &never, p.flags, 1000000000ull);
-            break;
-        }
-        float amax = 0.f;
-        if (valid) {
-#pragma unroll 6
-            for (int j = 0; j < 2 * kChunks; ++j) {
-                const uint4 v = src[j];
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[e] << 16)),
-                                             fabsf(__uint_as_float(w4[e] & 0xffff0000u))));
-            }
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        int e2 = 0;
-        frexpf(amax, &e2);                              // amax = m * 2^e2, m in [0.5, 1)
-        int sigma = amax > 0.f ? 8 - e2 : 0;            // max |q| * 2^sigma in [128, 256)
-        sigma = sigma > 100 ? 100 : (sigma < -100 ? -100 : sigma);
-        const float scale = ldexpf(1.f, sigma);
         if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
-        uint8_t* qb = base + kOffQ + qs * kQBytes;
-        // split each value into two E4M3 terms
-#pragma unroll 2
-        for (int cc16 = 0; cc16 < kChunks; ++cc16) {
-            const uint4 va = valid ? src[2 * cc16] : make_uint4(0, 0, 0, 0);
-            const uint4 vb = valid ? src[2 * cc16 + 1] : make_uint4(0, 0, 0, 0);
-            const uint32_t w8[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
-            uint32_t t1[4], t2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                uint32_t lo1 = 0, lo2 = 0;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t w = w8[2 * e + hh];
-                    const float x0 = __uint_as_float(w << 16) * scale;
-                    const float x1 = __uint_as_float(w & 0xffff0000u) * scale;
-                    const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
-                    const float2 d = e4m3x2_to_float2(b1);
-                    const uint16_t b2 = f32x2_to_e4m3x2(x0 - d.x, x1 - d.y);
-                    lo1 |= static_cast<uint32_t>(b1) << (16 * hh);
-                    lo2 |= static_cast<uint32_t>(b2) << (16 * hh);
-                }
-                t1[e] = lo1;
-                t2[e] = lo2;
-            }
-            const int c = c0 + cc16;
-            const int row1 = r, row2 = kHeadsPerCta + r;
-            uint8_t *d1, *d2;
-            if (c < 32) {                               // c_kv: 128-byte rows, 128-byte swizzle
-                const int cb = c >> 3, cc = c & 7;
-                d1 = qb + cb * kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4);
-                d2 = qb + cb * kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4);
-            } else {                                    // k_pe: 64-byte rows, 64-byte swizzle
-                const int cc = c - 32;
-                d1 = qb + 4 * kQBlk + row1 * 64 + ((cc ^ ((row1 >> 1) & 3)) << 4);
-                d2 = qb + 4 * kQBlk + row2 * 64 + ((cc ^ ((row2 >> 1) & 3)) << 4);
-            }
-            *reinterpret_cast<uint4*>(d1) = make_uint4(t1[0], t1[1], t1[2], t1[3]);
-            *reinterpret_cast<uint4*>(d2) = make_uint4(t2[0], t2[1], t2[2], t2[3]);
-        }
-        if ((lane & 1) == 0)
-            coefs[qs * kHeadsPerCta + r] =
-                valid ? ldexpf(p.softmax_scale * p.k_scale * kLog2e, -sigma) : 0.f;
-        // the raw rows may be overwritten by the next segment's copy and the
-        // split terms are read by the tensor core: both are async-proxy uses
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[Q_FULL + qs]);
+        const uint8_t* img = p.qimg + int64_t(sg.b) * kTcQImageBytes;
+        mbar_arrive_expect_tx(&bars[Q_FULL + qs], kTcQImageBytes);
+        bulk_copy_g2s(smem_u32(base + kOffQ + qs * kQBytes), img, kQBytes, &bars[Q_FULL + qs]);
+        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * kHeadsPerCta * 4), img + kQBytes, kHeadsPerCta * 4,
+                      &bars[Q_FULL + qs]);
         ++k;
     }
+    // copies in flight (after an abort) land before the CTA exits
+    volatile int never = 0;
+    for (int j = k - 2 < 0 ? 0 : k - 2; j < k; ++j)
+        mbar_wait(&bars[Q_FULL + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, &never, p.flags, 1000000000ull);
 }
 
 // ------------------------------------------------- softmax / rescale WG
@@ -800,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
         // KV_FULL: 32 cp.async arrivals from each fill warp; SL_EMPTY: fill
         // warps 1-3 and the four softmax warps
         const uint32_t counts[SL_FULL] = {32 * kFillWarps, 32 * kFillWarps, 1, 1, 1, 1, 128, 128,
-                                          128, 128, 1, 1, 128, 128, 1, 1, 129, 129, 1, 1};
+                                          128, 128, 1, 1, 128, 128, 1, 1, 129, 129, 1};
         for (int b = 0; b < SL_FULL; ++b) mbar_init(&bars[b], counts[b]);
         for (int e = 0; e < kRing; ++e) {
             mbar_init(&bars[SL_FULL + e], 1);
@@ -835,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
         }
         __syncwarp();
     } else if (warp == kWarpQ) {
-        q_prep(p, base, bars, abort, seg_lo, seg_hi, head0, lane);
+        q_fetch(p, base, bars, abort, seg_lo, seg_hi, lane);
     } else {
         WgCtx w;
         w.base = base;
@@ -876,8 +883,22 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
     }
     // slots are held as int32 in the kernel's shared slot lists
     if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
-    mla_decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    const int split_blocks = (p.batch * kHeadsPerCta * 32 + kSplitThreads - 1) / kSplitThreads;
+    mla_q_split_kernel<<<split_blocks, kSplitThreads, 0, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the decode kernel starts while the split runs: only its q warp waits
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
 }
 
 }  // namespace mla

@@ -121,6 +121,10 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
     s.partial_lse_offset = align256(o_bytes);
     s.workspace_bytes =
         s.n_partials ? align256(s.partial_lse_offset + static_cast<size_t>(s.n_partials) * H * 4) : 0;
+    if (kernel == DecodeKernel::kTc && s.num_ctas > 0) {
+        s.qimg_offset = s.workspace_bytes;
+        s.workspace_bytes = align256(s.qimg_offset + static_cast<size_t>(B) * kTcQImageBytes);
+    }
     return MLA_OK;
 }
 

@@ -15,6 +15,9 @@ namespace mla {
 constexpr int kTileTokens = 64;
 constexpr int kTcTileTokens = 128;
 constexpr int kHeadsPerCta = 16;
+// tcgen05 path: per request, [q1;q2] as the shared-memory image the MMA reads
+// (2 x 16 rows x 576 E4M3, swizzled) followed by 16 fp32 score multipliers
+constexpr int kTcQImageBytes = 2 * kHeadsPerCta * 576 + kHeadsPerCta * 4;
 
 // Which decode kernel a plan launches.
 enum class DecodeKernel : int32_t {
@@ -41,6 +44,7 @@ struct Schedule {
     int32_t n_partials = 0;
     int64_t n_tokens = 0;
     size_t partial_lse_offset = 0;   // bytes into the workspace
+    size_t qimg_offset = 0;          // tcgen05 path: q images, batch x kTcQImageBytes
     size_t workspace_bytes = 0;
 
     int32_t n_segs() const { return static_cast<int32_t>(segs.size() / 4); }
