@@ -234,7 +234,11 @@ def run_ours(args, rank, world, local):
         plan = M.mla_decode_plan(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3, stream=stream)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     info = M.mla_decode_plan_info(plan)
-    launches_per_call = 1 + (1 if info["num_partials"] > 0 else 0)
+    # per call: the tensor-core path (FP8, H <= 16, 128-token tiles) runs a q
+    # split and the decode, the mma.sync path the decode alone; both add the
+    # merge kernel when requests are split
+    tc_path = M.mla_decode_schedule(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3)[1]["tile_tokens"] == 128
+    launches_per_call = (2 if tc_path else 1) + (1 if info["num_partials"] > 0 else 0)
 
     def store(l, s):
         M.kv_store_fp8(new_ckv[l], new_kpe[l], slots_d, k_scales[l], pools[l, :, :512],

@@ -627,6 +627,9 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
     const float* coefs = reinterpret_cast<const float*>(w.base + kOffCoef);
     uint8_t* pbase = w.base + kOffP;
     const int32_t* ring = reinterpret_cast<const int32_t*>(w.base + kOffRing);
+    // A failed (aborted) wait is not a reason to leave: the softmax warps meet
+    // at named barriers, so all of them run the loops to the end; once the
+    // abort flag is set every wait returns at once and the results are void.
     int i = 0, k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
@@ -634,7 +637,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         const int qs = k & 1;
         const uint32_t qu = static_cast<uint32_t>(k) >> 1;
         const uint32_t ocol = kColO + 128 * (k & 1);
-        if (!mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags)) return;
+        mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags);
         // the segment's score multipliers stay in shared memory (q buffer qs
         // is released at the end of the segment)
         const float* coef = coefs + qs * kHeadsPerCta;
@@ -650,12 +653,11 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             const uint32_t u = static_cast<uint32_t>(i) >> 1;
             // row validity from the scheduler's slot list (a -1 row is zero-filled)
             const int e = i % kRing;
-            if (!mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, w.abort, w.flags))
-                return;
+            mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, w.abort, w.flags);
             const bool valid = ring[e * kTT + w.row] >= 0;
             __syncwarp();
             if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
-            if (!mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags)) return;
+            mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
             fence_after_sync();
             uint32_t r1[16], r2[16];
             tmem_ld16(w.tmem_lane + kColS + 32 * slot, r1);
@@ -695,16 +697,14 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                 if (it > 0) {
                     // O holds tiles up to i - 1: rescale once PV(i - 1) has landed
                     const int j = i - 1;
-                    if (!mbar_wait(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort,
-                                   w.flags))
-                        return;
+                    mbar_wait(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort, w.flags);
                     fence_after_sync();
                     rescale_o(w, ocol, alpha);
                 }
             }
             // P = 2^(s - m) <= 2^kTau, stored as two E4M3 terms of p * kPScale;
             // its buffer was last read by PV(i - 2)
-            if (i >= 2 && !mbar_wait(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags)) return;
+            if (i >= 2) mbar_wait(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags);
             uint32_t pk1[4], pk2[4];
 #pragma unroll
             for (int e4 = 0; e4 < 4; ++e4) {
@@ -752,8 +752,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
 #pragma unroll
         for (int h = 0; h < 16; ++h) inv[h] = l[h] > 0.f ? p.k_scale / l[h] : 0.f;
         const int jl = i - 1;                       // the segment's last tile
-        if (!mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags))
-            return;
+        mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
         const int H = p.heads;
         // o and l are both in units of p * kPScale; lse = m + log2(sum p)
