@@ -19,9 +19,11 @@
 // terms are stacked along N, so one MMA computes both partial products and
 // reads the cache tile once.
 //
-// Tile = 128 tokens = the MMA's M.  Per tile:
-//   S^T[128 x 32]  = K_tile[128 x 576] . [q1;q2]^T    18 MMAs, K-major A/B
-//   O^T[512 x 32] += V^T[512 x 128] . [P1;P2]^T       16 MMAs, MN-major A/B
+// Tile = 64 tokens = the QK^T MMA's M.  Per tile:
+//   S^T[64 x 32]   = K_tile[64 x 576] . [q1;q2]^T     18 MMAs, K-major A/B
+//   O^T[512 x 32] += V^T[512 x 64] . [P1;P2]^T        8 MMAs, MN-major A/B
+// A 64-token tile (36 KB) keeps four tiles in flight in 144 KB of shared
+// memory, which hides a tile's fill -> QK^T -> softmax -> PV round trip.
 // The same swizzled smem tile serves as K-major A (tokens x dims) and
 // MN-major A (dims x tokens).  S (double-buffered per tile) and O (one
 // accumulator per segment, double-buffered across segments) live in TMEM.
@@ -33,25 +35,26 @@
 // softmax warps rescale it in place before the next PV may add to it.
 //
 // Warp roles (one CTA per SM, persistent over its token range):
-//   warp 0     schedules tiles kAhead ahead of the stage fills: resolves each
-//              row's pool slot (or -1: past the context, outside the pool)
-//              into a small shared ring and has L2 prefetch the rows' cache
-//              lines, so the fills below read L2 rather than wait on DRAM;
-//   warps 0-3  fill a 2-stage ring with 16-byte cp.async: warp w copies
+//   warp 11    publishes tiles ahead of the stage fills: resolves each row's
+//              pool slot (or -1: past the context, outside the pool) into a
+//              small shared ring and has L2 prefetch the rows' cache lines,
+//              so the fills below read L2 rather than wait on DRAM;
+//   warps 0-3  fill a 4-stage ring with 16-byte cp.async: warp w copies
 //              c_kv channels 128w .. 128w+127 (128-byte swizzle) and a
 //              quarter of the k_pe rows (64-byte swizzle); an invalid row is
 //              zero-filled.  Measured on GB300, four LSU warps fed from L2
 //              gather at the HBM rate, which neither fewer warps nor TMA
 //              tile::gather4 reach;
-//   warp 4     one thread issues every tcgen05.mma and commit, polling so
-//              that PV of one tile and QK^T of the next go out in whichever
-//              order their inputs become ready;
+//   warp 4     one thread issues the QK^T MMAs, tile after tile;
+//   warp 10    one thread issues the PV MMAs, so that PV of one tile never
+//              waits behind QK^T of the next;
 //   warp 5     fetches each segment's [q1;q2] image and per-head score
 //              multipliers, written by the q split kernel that precedes this
 //              one (double-buffered);
-//   warps 6-9  one thread per TMEM lane: online softmax of a token's 16
-//              heads and the E4M3 split of P, rescaling O when the maximum
-//              moves, and the epilogue (lane = output channel).
+//   warps 6-9  online softmax of a token's 16 heads and the E4M3 split of P
+//              (an M = 64 accumulator puts a tile's rows in lanes 0-15 of
+//              each warp's TMEM lane quadrant), rescaling O when the maximum
+//              moves, and the epilogue (all lanes: lane = output channel).
 // Every mbarrier wait is bounded; on a timeout the CTA sets
 // MLA_FLAG_WAIT_TIMEOUT, drains its MMAs and copies, frees TMEM and exits.
 #include <mutex>
@@ -67,19 +70,21 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTT = kTcTileTokens;          // 128 tokens per tile (MMA M)
-constexpr int kM = 128;
-constexpr int kStages = 2;
+// Tiles are 64 tokens (the QK^T MMA's M): segments start on multiples of the
+// plan's 128-token granularity, so they also start on a tile.
+constexpr int kTT = 64;
+constexpr int kM = 64;
+constexpr int kStages = 4;
 constexpr int kFillWarps = 4;
-constexpr int kWarpMma = 4, kWarpQ = 5, kWarpWg = 6;
-constexpr int kThreads = 320;
-constexpr int kBlk = kTT * 128;             // 128 rows x 128 B, 128-byte swizzle (128 c_kv channels)
-constexpr int kRope = kTT * 64;             // 128 rows x 64 B, 64-byte swizzle (the 64 k_pe channels)
-constexpr int kStage = 4 * kBlk + kRope;    // 72 KB per tile
+constexpr int kWarpMma = 4, kWarpQ = 5, kWarpWg = 6, kWarpPv = 10, kWarpSched = 11;
+constexpr int kThreads = 384;
+constexpr int kBlk = kTT * 128;             // 64 rows x 128 B, 128-byte swizzle (128 c_kv channels)
+constexpr int kRope = kTT * 64;             // 64 rows x 64 B, 64-byte swizzle (the 64 k_pe channels)
+constexpr int kStage = 4 * kBlk + kRope;    // 36 KB per tile
 constexpr int kQRows = 2 * kHeadsPerCta;    // B rows: q1 of heads 0..15, then q2
 constexpr int kQBlk = kQRows * 128;         // 4 KB per 128-channel block
 constexpr int kQBytes = 4 * kQBlk + kQRows * 64;   // + the k_pe block: 18 KB
-constexpr int kPUnit = kTT * 16;            // one E4M3 term of P^T: 128 tokens x 16 heads
+constexpr int kPUnit = kTT * 16;            // one E4M3 term of P^T: 64 tokens x 16 heads
 constexpr int kPBytes = 2 * kPUnit;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;               // S[j]: columns 32j .. 32j+31
@@ -89,9 +94,8 @@ constexpr float kTau = 4.f;                 // lazy-rescale threshold (log2 unit
 constexpr float kPScale = 16.f;             // P is stored as p * 2^kTau
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kRing = 8;                    // scheduled tiles' slot lists in flight
-constexpr int kAhead = 3;                   // tiles published (and prefetched) beyond the one filling
-static_assert(kAhead + kStages < kRing, "the scheduler may not lap the softmax warps");
+constexpr int kRing = 8;                    // published tiles' slot lists (and L2 prefetches) in flight
+static_assert(kRing > kStages, "the ring covers the tiles the stages hold");
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffStage = 0;
@@ -108,8 +112,9 @@ constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(kBlk % 1024 == 0 && kStage % 1024 == 0 && kQBytes % 1024 == 0,
               "swizzle atoms need 1 KB alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
-static_assert(kTT == kM, "a tile fills the MMA's M exactly");
-static_assert(kThreads == 32 * (kWarpWg + 4), "four softmax warps after the others");
+static_assert(kTT == kM && kTcTileTokens % kTT == 0, "a tile fills the MMA's M; segments start on tiles");
+static_assert(kWarpPv == kWarpWg + 4 && kWarpSched == kWarpPv + 1 && kThreads == 32 * (kWarpSched + 1),
+              "warp roles");
 
 enum : int {
     KV_FULL = 0, KV_EMPTY = kStages, S_FULL = 2 * kStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
@@ -117,7 +122,8 @@ enum : int {
     DONE = Q_FREE + 2, SL_FULL = DONE + 1, SL_EMPTY = SL_FULL + kRing,
     NUM_BARS = SL_EMPTY + kRing
 };
-static_assert(NUM_BARS == 35 && NUM_BARS * 8 <= 512, "barrier count table below assumes two stages");
+static_assert(NUM_BARS * 8 <= 512, "barrier space");
+static_assert(SL_FULL == 23, "barrier count table below assumes four stages");
 
 struct Seg {
     int32_t b, t0, t1, part, ntiles;
@@ -150,7 +156,7 @@ __device__ __forceinline__ void wg_bar() { asm volatile("bar.sync 1, 128;\n" :::
 
 // ------------------------------------------------------------ producer warps
 //
-// Warp 0 walks the CTA's tiles kAhead ahead of the stage fills: it resolves
+// The scheduler warp walks the CTA's tiles ahead of the stage fills: it resolves
 // the 128 rows of a tile to pool slots, publishes them in a shared ring
 // (SL_FULL / SL_EMPTY) and has L2 prefetch each row's cache lines.  By the
 // time a stage frees up, the rows it needs are on their way to (or already
@@ -159,13 +165,13 @@ __device__ __forceinline__ void wg_bar() { asm volatile("bar.sync 1, 128;\n" :::
 constexpr int32_t kNoRow = INT32_MIN;
 
 // Cursor over the tiles of a CTA's segments, with the raw page entries of
-// rows 4 lane .. 4 lane + 3 of one tile.
+// rows 2 lane, 2 lane + 1 of one tile.
 struct TileCursor {
     int si, seg_hi, it;
     Seg sg;
     const int32_t* pages;
-    int32_t pg[4];                      // page entry, or kNoRow past the context
-    int32_t t[4];                       // token index of each row
+    int32_t pg[2];                      // page entry, or kNoRow past the context
+    int32_t t[2];                       // token index of each row
 
     __device__ void init(const DecodeParams& p, int lo, int hi) {
         si = lo;
@@ -179,15 +185,15 @@ struct TileCursor {
     // on them until rows() is called
     __device__ void prefetch(const DecodeParams& p, int lane) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            t[q] = sg.t0 + it * kTT + 4 * lane + q;
+        for (int q = 0; q < 2; ++q) {
+            t[q] = sg.t0 + it * kTT + 2 * lane + q;
             pg[q] = t[q] < sg.t1 ? pages[p.page_size == 1 ? t[q] : t[q] / p.page_size] : kNoRow;
         }
     }
     // slot of each row, or -1 (past the context or outside the pool: flagged)
-    __device__ void rows(const DecodeParams& p, int32_t (&slot)[4]) const {
+    __device__ void rows(const DecodeParams& p, int32_t (&slot)[2]) const {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const int64_t s = p.page_size == 1 ? int64_t(pg[q])
                                                : int64_t(pg[q]) * p.page_size + t[q] % p.page_size;
             const bool ok = pg[q] >= 0 && s < p.num_slots;
@@ -207,9 +213,9 @@ struct TileCursor {
 
 // Copies warp w's share of tile i into its stage: c_kv block w (8 chunks of
 // 16 B per row, four rows per instruction) and k_pe rows 8g .. 8g+7 for
-// g = w, w+4, w+8, w+12 (4 chunks per row, eight rows per instruction).
+// g = w, w+4 (4 chunks per row, eight rows per instruction).
 // `sl` holds the slots of rows lane + 32q.
-__device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage, const int32_t (&sl)[4],
+__device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage, const int32_t (&sl)[2],
                                            int w, int lane) {
     const int r4 = lane >> 3, c8 = lane & 7;
 #pragma unroll
@@ -232,25 +238,26 @@ __device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage
     }
 }
 
-__device__ void scheduler_fill(const DecodeParams& p, uint8_t* base, uint64_t* bars,
-                               volatile int* abort, int seg_lo, int seg_hi, int lane) {
+__device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
+                          int seg_lo, int seg_hi, int lane) {
     int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
     // one prefetch sweep per row when k_pe follows c_kv in the same row
     const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
     TileCursor cur;
     cur.init(p, seg_lo, seg_hi);
     if (cur.valid()) cur.prefetch(p, lane);
-    int n_sched = 0;
-    // publishes the cursor's tile in the ring and prefetches its rows to L2
-    auto schedule = [&]() -> bool {
-        const int e = n_sched % kRing;
-        const uint32_t u = static_cast<uint32_t>(n_sched / kRing);
-        int32_t sl[4];
+    // publishes every tile as soon as its ring entry is free (the ring bounds
+    // how far ahead of the softmax warps the prefetches run)
+    for (int n = 0; cur.valid(); ++n) {
+        const int e = n % kRing;
+        const uint32_t u = static_cast<uint32_t>(n / kRing);
+        int32_t sl[2];
         cur.rows(p, sl);
         cur.advance(p);
         if (cur.valid()) cur.prefetch(p, lane);       // the next tile's index loads fly meanwhile
+        if (!mbar_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             if (sl[q] < 0) continue;
             const uint8_t* row = p.ckv + int64_t(sl[q]) * p.ckv_stride;
             if (joint) {
@@ -260,30 +267,10 @@ __device__ void scheduler_fill(const DecodeParams& p, uint8_t* base, uint64_t* b
                 prefetch_row_l2<kDKpe>(p.kpe + int64_t(sl[q]) * p.kpe_stride);
             }
         }
-        if (!mbar_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) return false;
-        *reinterpret_cast<int4*>(ring + e * kTT + 4 * lane) = make_int4(sl[0], sl[1], sl[2], sl[3]);
+        *reinterpret_cast<int2*>(ring + e * kTT + 2 * lane) = make_int2(sl[0], sl[1]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[SL_FULL + e]);
-        ++n_sched;
-        return true;
-    };
-    // tile 0 is filled as soon as it is resolved; from tile 1 on, tiles up
-    // to i + kAhead are published once tile i's fill is under way
-    bool ok = !cur.valid() || schedule();
-    for (int i = 0; ok && i < n_sched; ++i) {
-        const int slot = i % kStages;
-        const uint32_t u = static_cast<uint32_t>(i / kStages);
-        const int e = i % kRing;
-        int32_t sl[4];                                // rows lane + 32 q (own writes: no wait)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
-        if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
-        fill_share(p, base + kOffStage + slot * kStage, sl, 0, lane);
-        mbar_arrive_cp_async(&bars[KV_FULL + slot]);
-        const int target = i == 0 ? 1 : i + kAhead;
-        while (ok && cur.valid() && n_sched <= target) ok = schedule();
     }
-    cp_async_wait<0>();
 }
 
 __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
@@ -295,9 +282,9 @@ __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
         const uint32_t u = static_cast<uint32_t>(i / kStages);
         const int e = i % kRing;
         if (!mbar_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, abort, p.flags)) break;
-        int32_t sl[4];
+        int32_t sl[2];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
+        for (int q = 0; q < 2; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[SL_EMPTY + e]);
         if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
@@ -387,73 +374,57 @@ struct SegWalk {
     }
 };
 
-// QK^T of tile i and PV of tile j < i are independent once their inputs are
-// ready; the issuer polls both and sends whichever is ready (PV first, since
-// it frees a stage for the next load).  QK^T runs at most one tile ahead.
-__device__ void mma_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
+// Two issuing threads: one sends QK^T of the tiles in order, the other PV.
+// A thread waits for each MMA it issues to be accepted, so with one issuer the
+// PV of tile i queued behind QK^T of tile i + 1 (and freed its stage late);
+// with two, each goes out as soon as its inputs are ready.  QK^T needs its
+// stage full, so it runs at most a stage ahead of PV by construction.
+__device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
     int total = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
         if (sg.ntiles == 0 && sg.t1 > sg.t0) raise_flag(p.flags, MLA_FLAG_PLAN_MISMATCH);
         total += sg.ntiles;
     }
-    SegWalk wq, wp;                    // QK and PV positions
+    SegWalk wq;
     wq.init(p, seg_lo, seg_hi);
-    wp.init(p, seg_lo, seg_hi);
-    int qk = 0, pv = 0;
-    uint64_t last = global_ns();
-    uint32_t spins = 0;
-    while (pv < total) {
-        bool did = false;
-        if (pv < qk) {
-            const uint32_t u = static_cast<uint32_t>(pv) >> 1;
-            const int ob = wp.k & 1;
-            const uint32_t ou = static_cast<uint32_t>(wp.k) >> 1;
-            if (mbar_test(&c.bars[P_FULL + (pv & 1)], u & 1) &&
-                (wp.it != 0 || mbar_test(&c.bars[O_FREE + ob], (ou & 1) ^ 1))) {
-                fence_after_sync();
-                fence_proxy_async_smem();
-                issue_pv(c, pv, ob, wp.it == 0);
-                wp.advance(p);
-                ++pv;
-                did = true;
-            }
-        }
-        if (!did && qk < total && qk - pv < 2) {
-            const int slot = qk & 1;
-            const uint32_t u = static_cast<uint32_t>(qk) >> 1;
-            const int qs = wq.k & 1;
-            const uint32_t qu = static_cast<uint32_t>(wq.k) >> 1;
-            const int kv = qk % kStages;
-            const uint32_t kvu = static_cast<uint32_t>(qk / kStages);
-            if ((wq.it != 0 || mbar_test(&c.bars[Q_FULL + qs], qu & 1)) &&
-                mbar_test(&c.bars[KV_FULL + kv], kvu & 1) &&
-                mbar_test(&c.bars[S_FREE + slot], (u & 1) ^ 1)) {
-                fence_after_sync();
-                fence_proxy_async_smem();
-                issue_qk(c, qk, qs);
-                if (wq.it == wq.sg.ntiles - 1) mma_commit(&c.bars[Q_FREE + qs]);   // q buffer done
-                wq.advance(p);
-                ++qk;
-                did = true;
-            }
-        }
-        if (did) {
-            spins = 0;
-            last = global_ns();
-        } else {
-            __nanosleep(32);
-        }
-        if (!did && (++spins & 63) == 0) {
-            if (*c.abort) break;
-            if (global_ns() - last > 2000000000ull) {
-                *c.abort = 1;
-                raise_flag(c.flags, MLA_FLAG_WAIT_TIMEOUT);
-                break;
-            }
-        }
+    for (int qk = 0; qk < total; ++qk) {
+        const int slot = qk & 1;
+        const int qs = wq.k & 1;
+        if (wq.it == 0 && !mbar_wait(&c.bars[Q_FULL + qs], (static_cast<uint32_t>(wq.k) >> 1) & 1, c.abort, c.flags))
+            break;
+        if (!mbar_wait(&c.bars[KV_FULL + qk % kStages], static_cast<uint32_t>(qk / kStages) & 1, c.abort, c.flags))
+            break;
+        if (!mbar_wait(&c.bars[S_FREE + slot], ((static_cast<uint32_t>(qk) >> 1) & 1) ^ 1, c.abort, c.flags))
+            break;
+        fence_after_sync();
+        fence_proxy_async_smem();
+        issue_qk(c, qk, qs);
+        if (wq.it == wq.sg.ntiles - 1) mma_commit(&c.bars[Q_FREE + qs]);   // q buffer done
+        wq.advance(p);
     }
     // every MMA issued so far has completed before TMEM may be released
+    mma_commit(&c.bars[DONE]);
+    volatile int never = 0;
+    mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
+}
+
+__device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
+    const int total = count_tiles(p, seg_lo, seg_hi);
+    SegWalk wp;
+    wp.init(p, seg_lo, seg_hi);
+    for (int pv = 0; pv < total; ++pv) {
+        const int ob = wp.k & 1;
+        if (!mbar_wait(&c.bars[P_FULL + (pv & 1)], (static_cast<uint32_t>(pv) >> 1) & 1, c.abort, c.flags)) break;
+        // a segment's first PV overwrites O buffer k & 1: segment k - 2 has been read out
+        if (wp.it == 0 &&
+            !mbar_wait(&c.bars[O_FREE + ob], ((static_cast<uint32_t>(wp.k) >> 1) & 1) ^ 1, c.abort, c.flags))
+            break;
+        fence_after_sync();
+        fence_proxy_async_smem();
+        issue_pv(c, pv, ob, wp.it == 0);
+        wp.advance(p);
+    }
     mma_commit(&c.bars[DONE]);
     volatile int never = 0;
     mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
@@ -578,7 +549,10 @@ struct WgCtx {
     uint32_t tmem_lane;     // TMEM base + this warp's lane quadrant
     volatile int* abort;
     uint32_t* flags;
-    int row;                // TMEM lane = token of a tile / channel of a block
+    int row;                // TMEM lane of O = channel within a 128-channel block
+    int srow;               // token of S (M = 64: lanes 0-15 of each lane quadrant)
+    int hb;                 // heads hb .. hb+7 of token srow are this lane's: lanes 0-15
+                            // take heads 0-7 and lanes 16-31 heads 8-15 of the same tokens
     int wq, lane;           // softmax warp 0..3, lane
 };
 
@@ -602,22 +576,22 @@ __device__ __forceinline__ void rescale_o(const WgCtx& w, uint32_t ocol, const f
     tmem_wait_st();
 }
 
-// Maximum over the 32 lanes of 16 values at once by halving exchanges
-// (16 shuffles instead of 80): afterwards lane l holds head l >> 1.
-__device__ __forceinline__ float warp_max16(const float (&v)[16], int lane) {
-    float a8[8], a4[4], a2[2];
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        a8[j] = fmaxf(b4 ? v[j + 8] : v[j], __shfl_xor_sync(0xffffffffu, b4 ? v[j] : v[j + 8], 16));
+// Reduction over the 16 lanes of a half warp of 8 values at once by halving
+// exchanges (8 shuffles instead of 32): afterwards lane l holds value
+// (l >> 1) & 7 reduced over its half.
+template <bool kMax>
+__device__ __forceinline__ float half_reduce8(const float (&v)[8], int lane) {
+    auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+    float a4[4], a2[2];
+    const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        a4[j] = fmaxf(b3 ? a8[j + 4] : a8[j], __shfl_xor_sync(0xffffffffu, b3 ? a8[j] : a8[j + 4], 8));
+        a4[j] = op(b3 ? v[j + 4] : v[j], __shfl_xor_sync(0xffffffffu, b3 ? v[j] : v[j + 4], 8));
 #pragma unroll
     for (int j = 0; j < 2; ++j)
-        a2[j] = fmaxf(b2 ? a4[j + 2] : a4[j], __shfl_xor_sync(0xffffffffu, b2 ? a4[j] : a4[j + 2], 4));
-    float a1 = fmaxf(b1 ? a2[1] : a2[0], __shfl_xor_sync(0xffffffffu, b1 ? a2[0] : a2[1], 2));
-    return fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+        a2[j] = op(b2 ? a4[j + 2] : a4[j], __shfl_xor_sync(0xffffffffu, b2 ? a4[j] : a4[j + 2], 4));
+    const float a1 = op(b1 ? a2[1] : a2[0], __shfl_xor_sync(0xffffffffu, b1 ? a2[0] : a2[1], 2));
+    return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
 }
 
 __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, int seg_hi, int head0) {
@@ -642,11 +616,11 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         // is released at the end of the segment)
         const float* coef = coefs + qs * kHeadsPerCta;
 
-        float m[16], l[16];
+        float m[8], l[8];                           // heads hb .. hb+7
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
+        for (int j = 0; j < 8; ++j) {
+            m[j] = -INFINITY;
+            l[j] = 0.f;
         }
         for (int it = 0; it < sg.ntiles; ++it, ++i) {
             const int slot = i & 1;
@@ -654,7 +628,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             // row validity from the scheduler's slot list (a -1 row is zero-filled)
             const int e = i % kRing;
             mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, w.abort, w.flags);
-            const bool valid = ring[e * kTT + w.row] >= 0;
+            const bool valid = ring[e * kTT + w.srow] >= 0;
             __syncwarp();
             if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
             mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
@@ -666,12 +640,16 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             fence_before_sync();
             mbar_arrive(&w.bars[S_FREE + slot]);
 
-            float s[16];
+            // lanes 0-15 hold the token's 16 heads; heads 8-15 move to lanes 16-31
+            float s[8];
             bool need = false;
 #pragma unroll
-            for (int h = 0; h < 16; ++h) {
-                s[h] = valid ? (__uint_as_float(r1[h]) + __uint_as_float(r2[h])) * coef[h] : -INFINITY;
-                need |= s[h] > m[h] + kTau;         // always true on a segment's first tile
+            for (int j = 0; j < 8; ++j) {
+                const float hi = __shfl_sync(0xffffffffu, __uint_as_float(r1[8 + j]) + __uint_as_float(r2[8 + j]),
+                                             w.lane & 15);
+                const float raw = w.hb ? hi : __uint_as_float(r1[j]) + __uint_as_float(r2[j]);
+                s[j] = valid ? raw * coef[w.hb + j] : -INFINITY;
+                need |= s[j] > m[j] + kTau;         // always true on a segment's first tile
             }
             // the running maximum moves only if some score got more than
             // 2^kTau above it (one vote per warp, then one barrier)
@@ -681,76 +659,79 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             wg_bar();
             need = vb[0] | vb[1] | vb[2] | vb[3];
             if (need) {
-                const float wmax = warp_max16(s, w.lane);
+                const float hmax = half_reduce8<true>(s, w.lane);
                 float* rb = red + (i & 1) * 64;
-                if ((w.lane & 1) == 0) rb[w.wq * 16 + (w.lane >> 1)] = wmax;
+                if ((w.lane & 1) == 0) rb[w.wq * 16 + w.hb + ((w.lane >> 1) & 7)] = hmax;
                 wg_bar();
-                float alpha[16];
+                float alpha[8];
 #pragma unroll
-                for (int h = 0; h < 16; ++h) {
+                for (int j = 0; j < 8; ++j) {
+                    const int h = w.hb + j;
                     const float tmax = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
-                    const float mn = fmaxf(m[h], tmax);
-                    alpha[h] = m[h] == -INFINITY ? 0.f : fast_exp2(m[h] - mn);
-                    m[h] = mn;
-                    l[h] *= alpha[h];
+                    const float mn = fmaxf(m[j], tmax);
+                    alpha[j] = m[j] == -INFINITY ? 0.f : fast_exp2(m[j] - mn);
+                    m[j] = mn;
+                    l[j] *= alpha[j];
                 }
                 if (it > 0) {
-                    // O holds tiles up to i - 1: rescale once PV(i - 1) has landed
+                    // O holds tiles up to i - 1: rescale once PV(i - 1) has landed;
+                    // every lane needs all 16 heads' factors (lanes 0 and 16 have them)
+                    float a16[16];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        a16[j] = __shfl_sync(0xffffffffu, alpha[j], 0);
+                        a16[8 + j] = __shfl_sync(0xffffffffu, alpha[j], 16);
+                    }
                     const int j = i - 1;
                     mbar_wait(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort, w.flags);
                     fence_after_sync();
-                    rescale_o(w, ocol, alpha);
+                    rescale_o(w, ocol, a16);
                 }
             }
             // P = 2^(s - m) <= 2^kTau, stored as two E4M3 terms of p * kPScale;
             // its buffer was last read by PV(i - 2)
             if (i >= 2) mbar_wait(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags);
-            uint32_t pk1[4], pk2[4];
+            uint32_t pk1[2], pk2[2];
 #pragma unroll
-            for (int e4 = 0; e4 < 4; ++e4) {
+            for (int e2 = 0; e2 < 2; ++e2) {
                 uint32_t w1 = 0, w2 = 0;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    const int h = 4 * e4 + 2 * hh;
-                    const float x0 = m[h] == -INFINITY ? 0.f : fast_exp2(s[h] - m[h]) * kPScale;
-                    const float x1 = m[h + 1] == -INFINITY ? 0.f : fast_exp2(s[h + 1] - m[h + 1]) * kPScale;
+                    const int j = 4 * e2 + 2 * hh;
+                    const float x0 = m[j] == -INFINITY ? 0.f : fast_exp2(s[j] - m[j]) * kPScale;
+                    const float x1 = m[j + 1] == -INFINITY ? 0.f : fast_exp2(s[j + 1] - m[j + 1]) * kPScale;
                     const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
                     const float2 d1 = e4m3x2_to_float2(b1);
                     const uint16_t b2 = f32x2_to_e4m3x2(x0 - d1.x, x1 - d1.y);
                     const float2 d2 = e4m3x2_to_float2(b2);
-                    l[h] += d1.x + d2.x;
-                    l[h + 1] += d1.y + d2.y;
+                    l[j] += d1.x + d2.x;
+                    l[j + 1] += d1.y + d2.y;
                     w1 |= static_cast<uint32_t>(b1) << (16 * hh);
                     w2 |= static_cast<uint32_t>(b2) << (16 * hh);
                 }
-                pk1[e4] = w1;
-                pk2[e4] = w2;
+                pk1[e2] = w1;
+                pk2[e2] = w2;
             }
-            uint8_t* pb = pbase + slot * kPBytes + w.row * 16;
-            *reinterpret_cast<uint4*>(pb) = make_uint4(pk1[0], pk1[1], pk1[2], pk1[3]);
-            *reinterpret_cast<uint4*>(pb + kPUnit) = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+            uint8_t* pb = pbase + slot * kPBytes + w.srow * 16 + w.hb;
+            *reinterpret_cast<uint2*>(pb) = make_uint2(pk1[0], pk1[1]);
+            *reinterpret_cast<uint2*>(pb + kPUnit) = make_uint2(pk2[0], pk2[1]);
             fence_proxy_async_smem();
             fence_before_sync();                    // orders a rescale's TMEM stores too
             mbar_arrive(&w.bars[P_FULL + slot]);
         }
 
         // ---- epilogue: denominators over the token lanes, normalise, store
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-#pragma unroll
-            for (int h = 0; h < 16; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
-        }
-        if (w.lane == 0) {
-#pragma unroll
-            for (int h = 0; h < 16; ++h) lsum[w.wq * 16 + h] = l[h];
+        {
+            const float hsum = half_reduce8<false>(l, w.lane);
+            if ((w.lane & 1) == 0) lsum[w.wq * 16 + w.hb + ((w.lane >> 1) & 7)] = hsum;
         }
         wg_bar();
-        float inv[16];
+        float inv[16], L[16];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) l[h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
+        for (int h = 0; h < 16; ++h) L[h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
         wg_bar();                                   // lsum is reused by the next segment
 #pragma unroll
-        for (int h = 0; h < 16; ++h) inv[h] = l[h] > 0.f ? p.k_scale / l[h] : 0.f;
+        for (int h = 0; h < 16; ++h) inv[h] = L[h] > 0.f ? p.k_scale / L[h] : 0.f;
         const int jl = i - 1;                       // the segment's last tile
         mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
@@ -784,11 +765,12 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         fence_before_sync();
         mbar_arrive(&w.bars[O_FREE + (k & 1)]);      // the next segment but one may overwrite O
         mbar_arrive(&w.bars[Q_FREE + qs]);
-        if (w.row == 0) {
+        if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb+7
             float* dst = sg.part < 0 ? p.lse + int64_t(sg.b) * H : p.part_lse + int64_t(sg.part) * H;
 #pragma unroll
-            for (int h = 0; h < 16; ++h)
-                if (head0 + h < H) dst[head0 + h] = (m[h] + log2f(l[h]) + lse_off) * kLn2;
+            for (int j = 0; j < 8; ++j)
+                if (head0 + w.hb + j < H)
+                    dst[head0 + w.hb + j] = (m[j] + log2f(w.hb ? L[8 + j] : L[j]) + lse_off) * kLn2;
         }
         ++k;
     }
@@ -803,14 +785,15 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        // KV_FULL: 32 cp.async arrivals from each fill warp; SL_EMPTY: fill
-        // warps 1-3 and the four softmax warps
-        const uint32_t counts[SL_FULL] = {32 * kFillWarps, 32 * kFillWarps, 1, 1, 1, 1, 128, 128,
-                                          128, 128, 1, 1, 128, 128, 1, 1, 129, 129, 1};
+        // KV_FULL: 32 cp.async arrivals from each fill warp; SL_EMPTY: the fill
+        // warps and the four softmax warps
+        const uint32_t counts[SL_FULL] = {32 * kFillWarps, 32 * kFillWarps, 32 * kFillWarps,
+                                          32 * kFillWarps, 1, 1, 1, 1, 1, 1, 128, 128, 128, 128,
+                                          1, 1, 128, 128, 1, 1, 129, 129, 2};
         for (int b = 0; b < SL_FULL; ++b) mbar_init(&bars[b], counts[b]);
         for (int e = 0; e < kRing; ++e) {
             mbar_init(&bars[SL_FULL + e], 1);
-            mbar_init(&bars[SL_EMPTY + e], (kFillWarps - 1) + 4);
+            mbar_init(&bars[SL_EMPTY + e], kFillWarps + 4);
         }
         *abort = 0;
         mbar_fence_init();
@@ -823,26 +806,27 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     const int seg_lo = p.cta_ptr[blockIdx.x], seg_hi = p.cta_ptr[blockIdx.x + 1];
     const int head0 = 0;                          // this kernel serves H <= 16
 
-    if (warp == 0) {
-        scheduler_fill(p, base, bars, abort, seg_lo, seg_hi, lane);
+    if (warp == kWarpSched) {
+        scheduler(p, base, bars, abort, seg_lo, seg_hi, lane);
     } else if (warp < kFillWarps) {
         fill_warp(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
-    } else if (warp == kWarpMma) {
+    } else if (warp == kWarpMma || warp == kWarpPv) {
         if (lane == 0) {
             MmaCtx c;
             c.sbase = smem_u32(base);
             c.tmem = tmem;
             c.idesc_qk = idesc_e4m3_f32(kTT, 32, false, false);
-            c.idesc_pv = idesc_e4m3_f32(kTT, 32, true, true);
+            c.idesc_pv = idesc_e4m3_f32(128, 32, true, true);   // M = 128 channels of a block
             c.bars = bars;
             c.abort = abort;
             c.flags = p.flags;
-            mma_issuer(p, c, seg_lo, seg_hi);
+            if (warp == kWarpMma) qk_issuer(p, c, seg_lo, seg_hi);
+            else pv_issuer(p, c, seg_lo, seg_hi);
         }
         __syncwarp();
     } else if (warp == kWarpQ) {
         q_fetch(p, base, bars, abort, seg_lo, seg_hi, lane);
-    } else {
+    } else {                                      // warps kWarpWg .. kWarpWg + 3
         WgCtx w;
         w.base = base;
         w.bars = bars;
@@ -851,6 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
         w.abort = abort;
         w.flags = p.flags;
         w.row = quad * 32 + lane;
+        w.srow = quad * 16 + (lane & 15);
+        w.hb = (lane >> 4) * 8;
         w.wq = warp - kWarpWg;
         w.lane = lane;
         softmax_wg(p, w, seg_lo, seg_hi, head0);
