@@ -234,10 +234,10 @@ def run_ours(args, rank, world, local):
         plan = M.mla_decode_plan(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3, stream=stream)
     ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
     info = M.mla_decode_plan_info(plan)
-    # per call: the tensor-core path (FP8, H <= 16, 128-token tiles) runs a q
+    # per call: the tensor-core path (FP8, H <= 16) runs a q
     # split and the decode, the mma.sync path the decode alone; both add the
     # merge kernel when requests are split
-    tc_path = M.mla_decode_schedule(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3)[1]["tile_tokens"] == 128
+    tc_path = M.mla_decode_schedule(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3)[1]["kernel"] == 1
     launches_per_call = (2 if tc_path else 1) + (1 if info["num_partials"] > 0 else 0)
 
     def store(l, s):

@@ -204,7 +204,11 @@ mla_status_t mla_decode_plan_info(mla_plan_t plan, int32_t* num_ctas,
  * up to `capacity` segments as int32 quintuples
  *     (cta, request, token_begin, token_end, partial_index or -1)
  * into segments_out (may be NULL), in launch order; tile_tokens receives the
- * kernel's tile (segments start on tile boundaries).  Validates exactly like
+ * kernel's tile (segments start on tile boundaries) and kernel the decode
+ * kernel the plan would launch: 0 = mma.sync (BF16 pools, or more than 16
+ * heads), 1 = tcgen05 on the E4M3 bytes (FP8 pools, up to 16 heads).  The
+ * mma.sync schedule gives each CTA an equal share of tiles; the tcgen05 one
+ * balances tiles plus a fixed cost per segment.  Validates exactly like
  * mla_decode_plan.  Output pointers may be NULL.
  */
 mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
@@ -214,7 +218,7 @@ mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
                                  int32_t* segments_out, int32_t capacity,
                                  int32_t* num_segments, int32_t* num_partials,
                                  int32_t* num_ctas, int32_t* tile_tokens,
-                                 size_t* workspace_bytes);
+                                 int32_t* kernel, size_t* workspace_bytes);
 
 /*
  * kv_store_fp8 -- quantize-on-store scatter ([P1] "Step 3", CastToFP8 in

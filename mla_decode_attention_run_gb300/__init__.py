@@ -61,7 +61,7 @@ def library():
     lib.mla_decode_plan_destroy.argtypes = [_P]
     lib.mla_decode_plan_info.argtypes = [_P, _PI32, _PI32, _PI32, ctypes.POINTER(_sz)]
     lib.mla_decode_schedule.argtypes = [_P, _P, _i32, _i32, _i32, ctypes.c_int, _i32, _P, _i32,
-                                        _PI32, _PI32, _PI32, _PI32, ctypes.POINTER(_sz)]
+                                        _PI32, _PI32, _PI32, _PI32, _PI32, ctypes.POINTER(_sz)]
     lib.kv_store_fp8.argtypes = [_P, _P, _P, _i64, _f32, _P, _i64, _P, _i64, _i64, _P]
     lib.kv_gather_cast.argtypes = [_P, _i64, _P, _i64, _i64, _P, _i64, _i32, _f32, _P, _P, _P]
     lib.mla_get_last_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
@@ -197,18 +197,20 @@ def mla_decode_plan_info(plan: Plan) -> dict:
 def mla_decode_schedule(kv_indptr_host, seq_lens_host, batch: int, num_heads: int,
                         page_size: int, kv_dtype: int = MLA_KV_FP8_E4M3, num_sms: int = 152):
     """Host-only schedule: returns (segments int32 [n, 5] = cta, request, t0,
-    t1, partial; info dict).  Raises MLAError on invalid input."""
+    t1, partial; info dict with kernel 0 = mma.sync, 1 = tcgen05).  Raises
+    MLAError on invalid input."""
     lib = library()
     indptr, lens = _host_i32(kv_indptr_host), _host_i32(seq_lens_host)
-    n, p, c, t, w = _i32(), _i32(), _i32(), _i32(), _sz()
+    n, p, c, t, k, w = _i32(), _i32(), _i32(), _i32(), _i32(), _sz()
     args = (indptr.ctypes.data, lens.ctypes.data, batch, num_heads, page_size, kv_dtype, num_sms)
-    outs = (ctypes.byref(n), ctypes.byref(p), ctypes.byref(c), ctypes.byref(t), ctypes.byref(w))
+    outs = (ctypes.byref(n), ctypes.byref(p), ctypes.byref(c), ctypes.byref(t), ctypes.byref(k),
+            ctypes.byref(w))
     _check(lib.mla_decode_schedule(*args, None, 0, *outs), "mla_decode_schedule")
     segs = np.zeros((max(n.value, 1), 5), np.int32)
     _check(lib.mla_decode_schedule(*args, segs.ctypes.data, n.value, *outs),
            "mla_decode_schedule")
     return segs[:n.value], dict(num_ctas=c.value, num_partials=p.value, tile_tokens=t.value,
-                                workspace_bytes=w.value)
+                                kernel=k.value, workspace_bytes=w.value)
 
 
 def kv_store_fp8(ckv_new, kpe_new, slots, k_scale: float, ckv_pool, kpe_pool,

@@ -6,6 +6,7 @@
 // The schedule balances work by tokens, not by requests: with contexts drawn
 // from [1024, 8192] a per-request split leaves SMs idle, so the tile list of
 // all requests is cut into equal contiguous ranges (one per CTA).
+#include <cstdint>
 #include <cstring>
 #include <new>
 
@@ -31,6 +32,70 @@ DecodeKernel pick_kernel(mla_kv_dtype_t dtype, int32_t heads) {
 
 // A CTA gets at least this many tiles when there is enough work.
 int64_t min_tiles_per_cta(DecodeKernel k) { return k == DecodeKernel::kTc ? 1 : 2; }
+
+// tcgen05 schedule: requests' tiles in order, cut into CTA ranges so that the
+// largest CTA cost (tiles + kTcSegmentCost per segment) is as small as
+// possible: binary search on the cost cap, greedy fill under it.
+int64_t fill_under_cap(const int32_t* seq, int32_t B, int64_t tile, int64_t cap, int64_t max_ctas,
+                       Schedule* out, std::vector<int32_t>* segs_per_req) {
+    int64_t c = 0, cost = 0;
+    bool any = false;
+    if (out) out->cta_ptr.assign(1, 0);
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t done = 0;
+        const int64_t tiles = (seq[b] + tile - 1) / tile;
+        while (done < tiles) {
+            const int64_t room = cap - cost - kTcSegmentCost;
+            if (room < 1) {
+                if (cost == 0) return INT64_MAX;            // cap below one tile + segment
+                if (++c >= max_ctas) return INT64_MAX;
+                cost = 0;
+                if (out) out->cta_ptr.push_back(static_cast<int32_t>(out->segs.size() / 4));
+                continue;
+            }
+            const int64_t k = tiles - done < room ? tiles - done : room;
+            if (out) {
+                int64_t t1 = (done + k) * tile;
+                if (t1 > seq[b]) t1 = seq[b];
+                out->segs.insert(out->segs.end(), {b, static_cast<int32_t>(done * tile),
+                                                   static_cast<int32_t>(t1), -1});
+                ++(*segs_per_req)[b];
+            }
+            cost += kTcSegmentCost + k;
+            done += k;
+            any = true;
+        }
+    }
+    return any ? c + 1 : 0;
+}
+
+void build_cost_balanced(const int32_t* seq, int32_t B, int64_t tile, int64_t max_ctas, Schedule& s,
+                         std::vector<int32_t>& segs_per_req) {
+    int64_t n_tiles = 0, n_req = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        n_tiles += (seq[b] + tile - 1) / tile;
+        n_req += seq[b] > 0;
+    }
+    s.segs.clear();
+    if (n_tiles == 0 || max_ctas < 1) {
+        s.num_ctas = 0;
+        s.cta_ptr.assign(1, 0);
+        return;
+    }
+    int64_t lo = (n_tiles + kTcSegmentCost * n_req + max_ctas - 1) / max_ctas;
+    if (lo < kTcSegmentCost + 1) lo = kTcSegmentCost + 1;
+    int64_t hi = n_tiles + kTcSegmentCost;                     // everything in one CTA
+    if (hi < lo) hi = lo;
+    while (lo < hi) {
+        const int64_t mid = lo + (hi - lo) / 2;
+        if (fill_under_cap(seq, B, tile, mid, max_ctas, nullptr, nullptr) != INT64_MAX) hi = mid;
+        else lo = mid + 1;
+    }
+    const int64_t used = fill_under_cap(seq, B, tile, lo, max_ctas, &s, &segs_per_req);
+    s.num_ctas = static_cast<int32_t>(used);
+    s.cta_ptr.resize(s.num_ctas + 1);
+    s.cta_ptr[s.num_ctas] = static_cast<int32_t>(s.segs.size() / 4);
+}
 
 }  // namespace
 
@@ -78,30 +143,34 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
     if (ctas > by_work) ctas = by_work;
     s.num_ctas = static_cast<int32_t>(ctas);
 
-    // request tile offsets in the concatenated tile list
-    std::vector<int64_t> first_tile(B + 1, 0);
-    for (int32_t b = 0; b < B; ++b)
-        first_tile[b + 1] = first_tile[b] + (seq[b] + tile - 1) / tile;
-
     std::vector<int32_t> segs_per_req(B, 0);
-    s.cta_ptr.assign(s.num_ctas + 1, 0);
-    int32_t b = 0;
-    for (int32_t c = 0; c < s.num_ctas; ++c) {
-        s.cta_ptr[c] = static_cast<int32_t>(s.segs.size() / 4);
-        const int64_t lo = n_tiles * c / s.num_ctas, hi = n_tiles * (c + 1) / s.num_ctas;
-        int64_t pos = lo;
-        while (pos < hi) {
-            while (first_tile[b + 1] <= pos) ++b;       // skips empty requests too
-            const int64_t end = hi < first_tile[b + 1] ? hi : first_tile[b + 1];
-            const int64_t t0 = (pos - first_tile[b]) * tile;
-            int64_t t1 = (end - first_tile[b]) * tile;
-            if (t1 > seq[b]) t1 = seq[b];
-            s.segs.insert(s.segs.end(), {b, static_cast<int32_t>(t0), static_cast<int32_t>(t1), -1});
-            ++segs_per_req[b];
-            pos = end;
+    if (kernel == DecodeKernel::kTc) {
+        build_cost_balanced(seq, B, tile, ctas, s, segs_per_req);
+    } else {
+        // request tile offsets in the concatenated tile list
+        std::vector<int64_t> first_tile(B + 1, 0);
+        for (int32_t b = 0; b < B; ++b)
+            first_tile[b + 1] = first_tile[b] + (seq[b] + tile - 1) / tile;
+
+        s.cta_ptr.assign(s.num_ctas + 1, 0);
+        int32_t b = 0;
+        for (int32_t c = 0; c < s.num_ctas; ++c) {
+            s.cta_ptr[c] = static_cast<int32_t>(s.segs.size() / 4);
+            const int64_t lo = n_tiles * c / s.num_ctas, hi = n_tiles * (c + 1) / s.num_ctas;
+            int64_t pos = lo;
+            while (pos < hi) {
+                while (first_tile[b + 1] <= pos) ++b;       // skips empty requests too
+                const int64_t end = hi < first_tile[b + 1] ? hi : first_tile[b + 1];
+                const int64_t t0 = (pos - first_tile[b]) * tile;
+                int64_t t1 = (end - first_tile[b]) * tile;
+                if (t1 > seq[b]) t1 = seq[b];
+                s.segs.insert(s.segs.end(), {b, static_cast<int32_t>(t0), static_cast<int32_t>(t1), -1});
+                ++segs_per_req[b];
+                pos = end;
+            }
         }
+        s.cta_ptr[s.num_ctas] = static_cast<int32_t>(s.segs.size() / 4);
     }
-    s.cta_ptr[s.num_ctas] = static_cast<int32_t>(s.segs.size() / 4);
 
     // partial slots: consecutive per request, in launch order
     std::vector<int32_t> first_partial(B, -1);
@@ -139,7 +208,7 @@ extern "C" mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
                                             int32_t* segments_out, int32_t capacity,
                                             int32_t* num_segments, int32_t* num_partials,
                                             int32_t* num_ctas, int32_t* tile_tokens,
-                                            size_t* workspace_bytes) {
+                                            int32_t* kernel, size_t* workspace_bytes) {
     Schedule s;
     const mla_status_t st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads,
                                                 page_size, kv_dtype, num_sms, s);
@@ -158,6 +227,7 @@ extern "C" mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
     if (num_partials) *num_partials = s.n_partials;
     if (num_ctas) *num_ctas = s.num_ctas;
     if (tile_tokens) *tile_tokens = s.tile_tokens;
+    if (kernel) *kernel = static_cast<int32_t>(s.kernel);
     if (workspace_bytes) *workspace_bytes = s.workspace_bytes;
     return MLA_OK;
 }

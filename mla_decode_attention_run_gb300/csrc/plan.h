@@ -13,7 +13,11 @@ namespace mla {
 // Tokens per KV tile of the mma.sync decode kernel, of the tcgen05 decode
 // kernel, and heads per CTA.
 constexpr int kTileTokens = 64;
-constexpr int kTcTileTokens = 128;
+constexpr int kTcTileTokens = 64;
+// tcgen05 kernel: a segment (q fetch, pipeline refill, epilogue) costs about
+// as much CTA time as this many tiles (measured on GB300); the schedule
+// balances tiles + this per segment across CTAs
+constexpr int kTcSegmentCost = 2;
 constexpr int kHeadsPerCta = 16;
 // tcgen05 path: per request, [q1;q2] as the shared-memory image the MMA reads
 // (2 x 16 rows x 576 E4M3, swizzled) followed by 16 fp32 score multipliers

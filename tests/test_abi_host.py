@@ -14,6 +14,7 @@ import workloads as W
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mla_decode.h")
 # [q1;q2] as 2 x 16 rows of 576 E4M3 bytes, then 16 fp32 score multipliers
 QIMAGE_BYTES = 2 * 16 * 576 + 16 * 4
+SEGMENT_COST = 2          # tiles' worth of CTA time the tcgen05 schedule charges per segment
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,7 +55,8 @@ def _indptr(lens, ps):
 def _check_schedule(segs, info, lens, heads, num_sms=152):
     lens = np.asarray(lens)
     tile = info["tile_tokens"]
-    assert tile in (64, 128)
+    assert tile == 64
+    tc = info["kernel"] == 1
     # every request's tokens are covered exactly once, in order
     for b in range(len(lens)):
         mine = segs[segs[:, 1] == b]
@@ -73,18 +75,28 @@ def _check_schedule(segs, info, lens, heads, num_sms=152):
     # partial indices are a permutation of 0..n-1
     parts = segs[segs[:, 4] >= 0, 4]
     assert np.array_equal(np.sort(parts), np.arange(info["num_partials"]))
-    # CTAs are contiguous and balanced to within one tile (+ request tails)
     ctas = info["num_ctas"]
     hg = (heads + 15) // 16
     assert ctas <= max(1, num_sms // hg)
     tiles = np.zeros(ctas, np.int64)
+    cost = np.zeros(ctas, np.int64)
     for c, b, t0, t1, _ in segs:
         tiles[c] += (t1 - t0 + tile - 1) // tile
-    assert tiles.max() - tiles.min() <= 1
+        cost[c] += (t1 - t0 + tile - 1) // tile + SEGMENT_COST
     assert np.all(np.diff(segs[:, 0]) >= 0)
+    if tc:
+        # tcgen05 schedule: the largest CTA cost (tiles + a fixed cost per
+        # segment) is within one segment of the even share
+        n_req = int(np.sum(lens > 0))
+        total = int(np.sum((lens + tile - 1) // tile)) + SEGMENT_COST * n_req
+        assert cost.max() <= -(-total // max(ctas, 1)) + SEGMENT_COST + 1
+        assert np.all(cost > 0)
+    else:
+        # mma.sync schedule: contiguous ranges balanced to within one tile
+        assert tiles.max() - tiles.min() <= 1
     ws = info["workspace_bytes"]
     need = info["num_partials"] * heads * (512 + 1) * 4
-    if tile == 128 and ctas > 0:           # tcgen05 path: one q image per request
+    if tc and ctas > 0:                    # tcgen05 path: one q image per request
         need += len(lens) * QIMAGE_BYTES
     assert ws >= need
     if need == 0:
@@ -121,8 +133,8 @@ def test_schedule_picks_the_fp8_tensor_core_kernel_for_small_head_counts():
     _, fp8_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_FP8_E4M3)
     _, bf16_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_BF16)
     _, fp8_32 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 32, 1, M.MLA_KV_FP8_E4M3)
-    assert fp8_16["tile_tokens"] == 128
-    assert bf16_16["tile_tokens"] == 64 and fp8_32["tile_tokens"] == 64
+    assert fp8_16["kernel"] == 1
+    assert bf16_16["kernel"] == 0 and fp8_32["kernel"] == 0
 
 
 def test_schedule_all_empty():
