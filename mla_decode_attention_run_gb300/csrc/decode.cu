@@ -389,6 +389,7 @@ __global__ void __launch_bounds__(128)
 mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int heads,
                  const float* __restrict__ part_o, const float* __restrict__ part_lse,
                  uint16_t* __restrict__ out, float* __restrict__ lse) {
+    griddep_wait();                                 // the decode kernel's partials are complete
     const int e = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * 4 + warp;
@@ -538,10 +539,23 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
         if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     }
     if (s.n_merge() > 0) {
-        const dim3 grid(s.n_merge(), (s.heads + 3) / 4);
-        mla_merge_kernel<<<grid, 128, 0, cs>>>(plan->dev_meta + plan->off_merge, s.n_merge(), s.heads,
-                                               p.part_o, p.part_lse, p.out, p.lse);
-        if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+        // a programmatic dependent of the decode kernel: its launch is
+        // processed while the decode's last CTAs finish, and its blocks wait
+        // on the device for the decode's partials
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(s.n_merge(), (s.heads + 3) / 4);
+        cfg.blockDim = dim3(128);
+        cfg.stream = cs;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, mla_merge_kernel, static_cast<const int32_t*>(plan->dev_meta + plan->off_merge),
+                               static_cast<int>(s.n_merge()), static_cast<int>(s.heads),
+                               static_cast<const float*>(p.part_o), static_cast<const float*>(p.part_lse), p.out,
+                               p.lse) != cudaSuccess)
+            return MLA_ERR_CUDA;
     }
     return MLA_OK;
 }

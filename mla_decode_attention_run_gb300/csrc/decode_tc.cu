@@ -845,6 +845,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     __syncthreads();
     fence_after_sync();
     if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+    // this CTA's work is done: the merge kernel may be launched once every
+    // CTA got here
+    if (tid == 0) griddep_launch_dependents();
 }
 
 std::mutex g_mu;
