@@ -338,7 +338,8 @@ def run_ours(args, rank, world, local):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": committed_traffic(workload_name),
-                     "kernel": "mla_decode_run (decode kernel + split-KV merge)",
+                     "kernel": "mla_decode_run: q split + tcgen05 decode + split-KV merge, timed together",
+                     "traffic_of": "mla_decode_tc_kernel (ncu, profiles/decode_traffic.json)",
                      "algorithmic_bytes_per_launch": call_bytes,
                      "peak_source": f"{peak_src} HBM copy bandwidth"},
     }
