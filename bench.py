@@ -382,6 +382,10 @@ def run_ours(args, rank, world, local):
         result["baselines"] = run_baselines(torch, M, args, stream, pools, q, out, lse, ws,
                                             k_scales, store, indptr, idx, lens, timed, dist, dev)
 
+    # ---- the other configurations' decode call, timed alone (rank 0)
+    if rank == 0 and not args.no_configs:
+        result["configs"] = measure_configs(torch, M, dev, stream)
+
     # ---- CPU oracle baseline (rank 0, one GPU)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_from_device(pools[0], q[0], indptr, idx, lens,
@@ -389,6 +393,71 @@ def run_ours(args, rank, world, local):
     del g_step, g_decode
     M.mla_decode_plan_destroy(plan)
     return result
+
+
+def measure_configs(torch, M, dev, stream):
+    """The single-stream (1 x 4,096 tokens) and 128-head (128 x 32,768 tokens,
+    page size 64, 2.4 GB pool) decode calls, each timed as a CUDA graph of
+    back-to-back calls on random E4M3 pools (timing needs no latents).  The
+    128-head call is also set against the measured BF16 tensor peak: it does
+    2,176 flops per token and head."""
+    peak, peak_src = measured_peaks()
+    tflops_peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            tflops_peak = float(json.load(f).get("bf16_tflops", 0)) or None
+    res = {}
+    for name, reps in (("single", 50), ("large_head", 4)):
+        w = W.make_workload(name, latent_requests=[])
+        B, H, ps = w.batch, w.heads, w.page_size
+        pool = torch.randint(0, 256, (w.num_slots, W.D_ALL), dtype=torch.uint8, device=dev)
+        pool[(pool & 0x7F) == 0x7F] = 0x3C
+        q = torch.randn(B, H, W.D_ALL, device=dev).to(torch.bfloat16)
+        out = torch.empty(B, H, 512, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(B, H, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            plan = M.mla_decode_plan(w.kv_indptr, w.seq_lens, B, H, ps, stream=stream)
+        ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+        ip, ix, ln = (torch.from_numpy(a).to(dev) for a in (w.kv_indptr, w.kv_indices, w.seq_lens))
+        kernel = M.mla_decode_schedule(w.kv_indptr, w.seq_lens, B, H, ps)[1]["kernel"]
+
+        def call(s):
+            M.mla_decode_run(plan, q, pool[:, :512], pool[:, 512:], w.num_slots, ip, ix, ln,
+                             w.k_scale, W.SOFTMAX_SCALE, out, lse, ws, stream=s)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call(stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(reps):
+                call(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            g.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(3):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (3 * reps)
+        nbytes = A.decode_call_bytes(w.seq_lens, H, ps)
+        flops = A.decode_call_flops(w.seq_lens, H)
+        r = {"batch": B, "heads": H, "page_size": ps, "tokens": int(w.seq_lens.sum()),
+             "kernel": "tcgen05" if kernel == 1 else "mma.sync", "us_per_call": round(us, 3),
+             "achieved_gbs": round(nbytes / us / 1e3, 1), "hbm_frac": round(nbytes / us / 1e3 / peak, 4),
+             "tflops": round(flops / us / 1e6, 2),
+             "l2": "the whole call fits in L2 (latency-bound)" if nbytes < 64e6 else "inputs larger than L2"}
+        if tflops_peak and name == "large_head":
+            r["tensor_frac"] = round(flops / us / 1e6 / tflops_peak, 4)
+            r["tensor_peak"] = "measured cuBLAS bf16 burst " + str(tflops_peak) + " TFLOP/s"
+        res[name] = r
+        M.mla_decode_plan_destroy(plan)
+        del pool, q, out, lse, ws, g
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, store, indptr, idx,
@@ -506,6 +575,7 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=W.NUM_LAYERS)
     ap.add_argument("--no-baselines", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
