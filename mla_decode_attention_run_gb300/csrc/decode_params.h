@@ -31,7 +31,8 @@ struct DecodeParams {
 };
 
 // Launches the q split kernel and then, as its programmatic dependent, the
-// tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` CTAs.
+// tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` token ranges x
+// p.head_groups.
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream);
 
 }  // namespace mla

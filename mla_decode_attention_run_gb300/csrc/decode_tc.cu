@@ -34,6 +34,10 @@
 // O accumulates in TMEM across a segment's tiles; when m does move, the
 // softmax warps rescale it in place before the next PV may add to it.
 //
+// A CTA serves 16 heads of its token range; more heads run as more CTAs
+// (grid.y = head group).  The groups of a token range start together, so
+// their repeated reads of the same rows mostly hit L2.
+//
 // Warp roles (one CTA per SM, persistent over its token range):
 //   warp 11    publishes tiles ahead of the stage fills: resolves each row's
 //              pool slot (or -1: past the context, outside the pool) into a
@@ -475,14 +479,17 @@ __device__ __forceinline__ float amax_bf16x8(const uint4& v, float a) {
 constexpr int kSplitThreads = 64;
 
 // One warp per (request, head row): lane c splits 16-channel chunk c of c_kv,
-// lanes 0-3 also chunk c of k_pe.  Heads >= H get zero rows and multiplier 0.
+// lanes 0-3 also chunk c of k_pe.  Heads are taken in groups of 16, one image
+// per (request, group); heads >= H get zero rows and multiplier 0.
 __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const DecodeParams p) {
     griddep_launch_dependents();                // the decode kernel may start loading KV now
     const int wg = (blockIdx.x * kSplitThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int b = wg / kHeadsPerCta, r = wg % kHeadsPerCta;
+    const int rows = p.head_groups * kHeadsPerCta;
+    const int b = wg / rows, head = wg % rows, r = head % kHeadsPerCta;
     if (b >= p.batch) return;
-    const bool valid = r < p.heads;
-    const uint4* src = reinterpret_cast<const uint4*>(p.q + int64_t(b) * p.q_sb + int64_t(valid ? r : 0) * p.q_sh);
+    const bool valid = head < p.heads;
+    const uint4* src =
+        reinterpret_cast<const uint4*>(p.q + int64_t(b) * p.q_sb + int64_t(valid ? head : 0) * p.q_sh);
     const uint4 z = make_uint4(0, 0, 0, 0);
     const uint4 va = valid ? src[2 * lane] : z, vb = valid ? src[2 * lane + 1] : z;
     const bool rope = lane < 4;
@@ -495,7 +502,7 @@ __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const Decode
     int sigma = amax > 0.f ? 8 - e2 : 0;            // max |q| * 2^sigma in [128, 256)
     sigma = sigma > 100 ? 100 : (sigma < -100 ? -100 : sigma);
     const float scale = ldexpf(1.f, sigma);
-    uint8_t* img = p.qimg + int64_t(b) * kTcQImageBytes;
+    uint8_t* img = p.qimg + (int64_t(b) * p.head_groups + head / kHeadsPerCta) * kTcQImageBytes;
     const int row1 = r, row2 = kHeadsPerCta + r;
     uint4 t1, t2;
     split_chunk(va, vb, scale, t1, t2);
@@ -528,7 +535,7 @@ __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, vo
         const int qs = k & 1;
         const uint32_t qu = static_cast<uint32_t>(k) >> 1;
         if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
-        const uint8_t* img = p.qimg + int64_t(sg.b) * kTcQImageBytes;
+        const uint8_t* img = p.qimg + (int64_t(sg.b) * p.head_groups + blockIdx.y) * kTcQImageBytes;
         mbar_arrive_expect_tx(&bars[Q_FULL + qs], kTcQImageBytes);
         bulk_copy_g2s(smem_u32(base + kOffQ + qs * kQBytes), img, kQBytes, &bars[Q_FULL + qs]);
         bulk_copy_g2s(smem_u32(base + kOffCoef + qs * kHeadsPerCta * 4), img + kQBytes, kHeadsPerCta * 4,
@@ -804,7 +811,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int seg_lo = p.cta_ptr[blockIdx.x], seg_hi = p.cta_ptr[blockIdx.x + 1];
-    const int head0 = 0;                          // this kernel serves H <= 16
+    const int head0 = blockIdx.y * kHeadsPerCta;  // heads head0 .. head0 + 15 of every request
 
     if (warp == kWarpSched) {
         scheduler(p, base, bars, abort, seg_lo, seg_hi, lane);
@@ -871,13 +878,14 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
     }
     // slots are held as int32 in the kernel's shared slot lists
     if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
-    const int split_blocks = (p.batch * kHeadsPerCta * 32 + kSplitThreads - 1) / kSplitThreads;
+    const int split_blocks =
+        (p.batch * p.head_groups * kHeadsPerCta * 32 + kSplitThreads - 1) / kSplitThreads;
     mla_q_split_kernel<<<split_blocks, kSplitThreads, 0, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the decode kernel starts while the split runs: only its q warp waits
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = dim3(grid, p.head_groups);         // token ranges x 16-head groups
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;

@@ -23,15 +23,16 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 // Resident decode CTAs per SM (both kernels' shared-memory budgets allow one).
 int ctas_per_sm(DecodeKernel) { return 1; }
 
-// The tcgen05 kernel covers FP8 pools with up to 16 heads; the mma.sync
-// kernel everything else (more heads in groups of 16, BF16 pools).
-DecodeKernel pick_kernel(mla_kv_dtype_t dtype, int32_t heads) {
-    return (dtype == MLA_KV_FP8_E4M3 && heads <= kHeadsPerCta) ? DecodeKernel::kTc
-                                                               : DecodeKernel::kMma;
+// The tcgen05 kernel covers FP8 pools (16 heads per CTA, more heads as more
+// CTAs); the mma.sync kernel BF16 pools.
+DecodeKernel pick_kernel(mla_kv_dtype_t dtype, int32_t) {
+    return dtype == MLA_KV_FP8_E4M3 ? DecodeKernel::kTc : DecodeKernel::kMma;
 }
 
-// A CTA gets at least this many tiles when there is enough work.
-int64_t min_tiles_per_cta(DecodeKernel k) { return k == DecodeKernel::kTc ? 1 : 2; }
+// A CTA gets at least this many tiles when there is enough work (a tcgen05
+// CTA spends a few microseconds filling its pipeline, and every split of a
+// request adds a partial to merge).
+int64_t min_tiles_per_cta(DecodeKernel k) { return k == DecodeKernel::kTc ? 4 : 2; }
 
 // tcgen05 schedule: requests' tiles in order, cut into CTA ranges so that the
 // largest CTA cost (tiles + kTcSegmentCost per segment) is as small as
@@ -192,7 +193,8 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
         s.n_partials ? align256(s.partial_lse_offset + static_cast<size_t>(s.n_partials) * H * 4) : 0;
     if (kernel == DecodeKernel::kTc && s.num_ctas > 0) {
         s.qimg_offset = s.workspace_bytes;
-        s.workspace_bytes = align256(s.qimg_offset + static_cast<size_t>(B) * kTcQImageBytes);
+        s.workspace_bytes =
+            align256(s.qimg_offset + static_cast<size_t>(B) * s.head_groups * kTcQImageBytes);
     }
     return MLA_OK;
 }

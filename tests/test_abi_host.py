@@ -96,8 +96,8 @@ def _check_schedule(segs, info, lens, heads, num_sms=152):
         assert tiles.max() - tiles.min() <= 1
     ws = info["workspace_bytes"]
     need = info["num_partials"] * heads * (512 + 1) * 4
-    if tc and ctas > 0:                    # tcgen05 path: one q image per request
-        need += len(lens) * QIMAGE_BYTES
+    if tc and ctas > 0:                    # tcgen05 path: one q image per request and head group
+        need += len(lens) * hg * QIMAGE_BYTES
     assert ws >= need
     if need == 0:
         assert ws == 0
@@ -128,13 +128,13 @@ def test_schedule_ragged_and_empty_requests():
     _check_schedule(segs, info, lens, 4, num_sms=5)
 
 
-def test_schedule_picks_the_fp8_tensor_core_kernel_for_small_head_counts():
+def test_schedule_picks_the_tensor_core_kernel_for_fp8_pools():
     lens = np.array([1000, 3000])
     _, fp8_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_FP8_E4M3)
     _, bf16_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_BF16)
     _, fp8_32 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 32, 1, M.MLA_KV_FP8_E4M3)
-    assert fp8_16["kernel"] == 1
-    assert bf16_16["kernel"] == 0 and fp8_32["kernel"] == 0
+    assert fp8_16["kernel"] == 1 and fp8_32["kernel"] == 1
+    assert bf16_16["kernel"] == 0
 
 
 def test_schedule_all_empty():
