@@ -379,8 +379,16 @@ def run_ours(args, rank, world, local):
 
     # ---- the two baselines the pages describe, per decode step
     if not args.no_baselines:
-        result["baselines"] = run_baselines(torch, M, args, stream, pools, q, out, lse, ws,
-                                            k_scales, store, indptr, idx, lens, timed, dist, dev)
+        base = run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, store,
+                             indptr, idx, lens, timed, dist, dev)
+        ledger = base.pop("ledger")
+        # the fused step's graph (store + decode per layer) without the host plan
+        with torch.cuda.stream(stream):
+            t_graph = reduce_max(timed(g_step.replay, args.steps), dist, dev) / args.steps
+        ledger["fused_fp8"] = category_ledger(t_graph, {"store": base.pop("store_ms"),
+                                                        "attention": t_dec / args.steps})
+        result["baselines"] = base
+        result["ledger"] = ledger
 
     # ---- the other configurations' decode call, timed alone (rank 0)
     if rank == 0 and not args.no_configs:
@@ -460,6 +468,22 @@ def measure_configs(torch, M, dev, stream):
     return res
 
 
+def category_ledger(step_ms, parts):
+    """Per-step category ledger: each category's time (a graph of only that
+    category's launches over the step's layers), its share of the step, and
+    the step time if that category cost nothing.  Tags follow the launching
+    call: kv_store_fp8 -> store, the PyTorch full-pool .to(bfloat16) -> cast,
+    kv_gather_cast -> gather, mla_decode_run (q split, decode, merge) ->
+    attention.  'other' is what the categories alone do not account for
+    (gaps between launches, overlap)."""
+    out = {"step_ms": round(step_ms, 4), "categories": {}}
+    for k, v in parts.items():
+        out["categories"][k] = {"ms": round(v, 4), "share": round(v / step_ms, 4),
+                                "step_ms_if_free": round(max(step_ms - v, 0.0), 4)}
+    out["other_ms"] = round(step_ms - sum(parts.values()), 4)
+    return out
+
+
 def run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, store, indptr, idx,
                   lens, timed, dist, dev):
     L, B, P = args.layers, args.batch, W.POOL_SLOTS
@@ -486,22 +510,48 @@ def run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, stor
         M.mla_decode_run(plan_bf16, q[l], compact[:, :512], compact[:, 512:], n, indptr_d, seq_d,
                          lens_d, k_scales[l], sm, out[l], lse[l], ws_b, stream=s)
 
-    res = {}
-    for name, layer_fn in (("full_pool_cast_then_bf16_decode", cast_layer),
-                           ("gather_then_cast_then_bf16_decode", gather_layer)):
+    def cast_only(l, s):
+        full.copy_(pools[l].view(torch.float8_e4m3fn))
+
+    def gather_only(l, s):
+        M.kv_gather_cast(pools[l, :, :512], pools[l, :, 512:], idx_d, 1, 1.0, compact[:, :512],
+                         compact[:, 512:], stream=s)
+
+    def cast_attention(l, s):
+        M.mla_decode_run(plan_bf16, q[l], full[:, :512], full[:, 512:], P, indptr_d, idx_d,
+                         lens_d, k_scales[l], sm, out[l], lse[l], ws_b, stream=s)
+
+    def gather_attention(l, s):
+        M.mla_decode_run(plan_bf16, q[l], compact[:, :512], compact[:, 512:], n, indptr_d, seq_d,
+                         lens_d, k_scales[l], sm, out[l], lse[l], ws_b, stream=s)
+
+    def step_ms(*layer_fns):
+        """ms per step of a graph of L layers, each running layer_fns in order."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             s = torch.cuda.current_stream()
             for l in range(L):
-                store(l, s)
-                layer_fn(l, s)
+                for fn in layer_fns:
+                    fn(l, s)
         with torch.cuda.stream(stream):
             for _ in range(2):
                 g.replay()
             k = max(3, min(args.steps, 5))
             t = reduce_max(timed(g.replay, k), dist, dev)
-        res[name] = {"decode_step_ms": round(t / k, 3)}
         del g
+        return t / k
+
+    res, ledger = {}, {}
+    store_ms = step_ms(store)
+    for name, layer_fn, tag, only, attention in (
+            ("full_pool_cast_then_bf16_decode", cast_layer, "cast", cast_only, cast_attention),
+            ("gather_then_cast_then_bf16_decode", gather_layer, "gather", gather_only, gather_attention)):
+        t = step_ms(store, layer_fn)
+        res[name] = {"decode_step_ms": round(t, 3)}
+        ledger[name] = category_ledger(t, {"store": store_ms, tag: step_ms(only),
+                                           "attention": step_ms(attention)})
+    res["ledger"] = ledger
+    res["store_ms"] = store_ms
     cast_bytes = A.full_pool_cast_bytes(P) * L
     gather_bytes = A.gather_cast_bytes(n, n) * L
     res["full_pool_cast_then_bf16_decode"]["cast_bytes_per_step"] = cast_bytes
