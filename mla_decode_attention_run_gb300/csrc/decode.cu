@@ -520,6 +520,7 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
     p.flags = device_flags_ptr();
     p.qimg = static_cast<uint8_t*>(workspace) + s.qimg_offset;
     p.batch = s.batch;
+    p.group_heads = s.group_heads;
 
     if (s.kernel == DecodeKernel::kTc && num_pool_slots >= INT32_MAX) return MLA_ERR_UNSUPPORTED;
     if (s.num_ctas > 0 && s.kernel == DecodeKernel::kTc) {

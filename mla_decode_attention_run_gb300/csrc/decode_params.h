@@ -28,6 +28,7 @@ struct DecodeParams {
     uint32_t* flags;            // library flag word
     uint8_t* qimg;              // tcgen05 path: per-request q images (workspace)
     int32_t batch;
+    int32_t group_heads;        // tcgen05 path: heads per CTA (16 or 32); grid.y = head_groups
 };
 
 // Launches the q split kernel and then, as its programmatic dependent, the

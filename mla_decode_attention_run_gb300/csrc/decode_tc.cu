@@ -85,14 +85,9 @@ constexpr int kThreads = 384;
 constexpr int kBlk = kTT * 128;             // 64 rows x 128 B, 128-byte swizzle (128 c_kv channels)
 constexpr int kRope = kTT * 64;             // 64 rows x 64 B, 64-byte swizzle (the 64 k_pe channels)
 constexpr int kStage = 4 * kBlk + kRope;    // 36 KB per tile
-constexpr int kQRows = 2 * kHeadsPerCta;    // B rows: q1 of heads 0..15, then q2
-constexpr int kQBlk = kQRows * 128;         // 4 KB per 128-channel block
-constexpr int kQBytes = 4 * kQBlk + kQRows * 64;   // + the k_pe block: 18 KB
-constexpr int kPUnit = kTT * 16;            // one E4M3 term of P^T: 64 tokens x 16 heads
-constexpr int kPBytes = 2 * kPUnit;
+constexpr int kPUnit = kTT * 16;            // 16 columns of P^T (one term, 16 heads) x 64 tokens
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;               // S[j]: columns 32j .. 32j+31
-constexpr uint32_t kColO = 64;              // O[b]: 64 + 128b + 32mb (mb = 128-channel block)
+constexpr uint32_t kColS = 0;               // S[j]: columns kN j .. kN j + kN - 1
 constexpr int kKSteps = kDQk / 32;          // 18 k-steps of 32 channels for QK
 constexpr float kTau = 4.f;                 // lazy-rescale threshold (log2 units)
 constexpr float kPScale = 16.f;             // P is stored as p * 2^kTau
@@ -101,20 +96,46 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kRing = 8;                    // published tiles' slot lists (and L2 prefetches) in flight
 static_assert(kRing > kStages, "the ring covers the tiles the stages hold");
 
-// shared memory map (offsets from a 1024-byte aligned base)
+// A CTA serves G = 16 or 32 heads (32 when H is a multiple of 32: one read of
+// a tile then feeds twice the heads, and an N = 64 MMA costs what N = 32 does).
+constexpr int kMaxG = 32;
+
+template <int G>
+struct Shape {
+    static constexpr int kN = 2 * G;                  // MMA N: both E4M3 terms of G heads
+    static constexpr int kQBlk = kN * 128;            // q rows x 128 B per 128-channel block
+    static constexpr int kQBytes = 4 * kQBlk + kN * 64;   // + the k_pe block
+    static constexpr int kQBufs = G == 16 ? 2 : 1;    // q buffers in shared memory
+    static constexpr int kOBufs = G == 16 ? 2 : 1;    // O accumulators in TMEM
+    static constexpr int kPBytes = (kN / 16) * kPUnit;    // [P1;P2]^T of one tile
+    static constexpr int kHL = G / 2;                 // heads per softmax lane
+    static constexpr uint32_t kColO = 2 * kN;         // TMEM: S[0], S[1], then O[b] + 4 kN b
+    static constexpr int kImage = kQBytes + G * 4;    // q image + score multipliers
+    static_assert(kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(kColO + kOBufs * 4 * kN <= kTmemCols, "TMEM columns");
+};
+
+// shared memory map (offsets from a 1024-byte aligned base), the same for
+// both head counts
+constexpr int kQRegion = 2 * Shape<16>::kQBytes;
+static_assert(Shape<16>::kQBufs * Shape<16>::kQBytes <= kQRegion &&
+              Shape<32>::kQBufs * Shape<32>::kQBytes <= kQRegion, "q region");
 constexpr int kOffStage = 0;
 constexpr int kOffQ = kOffStage + kStages * kStage;
-constexpr int kOffP = kOffQ + 2 * kQBytes;
-constexpr int kOffRing = kOffP + 2 * kPBytes;   // kRing x 128 slots (int32)
+constexpr int kOffP = kOffQ + kQRegion;
+constexpr int kOffRing = kOffP + 2 * Shape<kMaxG>::kPBytes;   // kRing x 64 slots (int32)
 constexpr int kOffBar = kOffRing + kRing * kTT * 4;
-constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x 16
-constexpr int kOffLsum = kOffRed + 512;     // softmax denominators: 4 warps x 16
-constexpr int kOffCoef = kOffLsum + 256;    // score multipliers: 2 x 16 (bulk-copy target)
-constexpr int kOffFlag = kOffCoef + 128;    // rescale votes: 2 x 4 warps
+constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x G
+constexpr int kOffLsum = kOffRed + 2 * 4 * kMaxG * 4;   // softmax denominators: 4 warps x G
+constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // score multipliers (bulk-copy target)
+constexpr int kOffFlag = kOffCoef + 2 * 16 * 4;         // rescale votes: 2 x 4 warps
 constexpr int kOffMisc = kOffFlag + 32;     // TMEM base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-static_assert(kBlk % 1024 == 0 && kStage % 1024 == 0 && kQBytes % 1024 == 0,
-              "swizzle atoms need 1 KB alignment");
+static_assert(Shape<16>::kQBufs * 16 * 4 <= 2 * 16 * 4 && Shape<32>::kQBufs * 32 * 4 <= 2 * 16 * 4,
+              "multiplier space");
+static_assert(Shape<16>::kImage == kTcQImageBytes && Shape<32>::kImage == 2 * kTcQImageBytes,
+              "q image sizes the plan reserves");
+static_assert(kBlk % 1024 == 0 && kStage % 1024 == 0, "swizzle atoms need 1 KB alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTT == kM && kTcTileTokens % kTT == 0, "a tile fills the MMA's M; segments start on tiles");
 static_assert(kWarpPv == kWarpWg + 4 && kWarpSched == kWarpPv + 1 && kThreads == 32 * (kWarpSched + 1),
@@ -316,22 +337,24 @@ __device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_of
     return base_desc + static_cast<uint64_t>(byte_offset >> 4);
 }
 
+template <int G>
 __device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
+    using S = Shape<G>;
     const int slot = i & 1;
     const uint32_t stage = c.sbase + kOffStage + (i % kStages) * kStage;
-    const uint32_t qb = c.sbase + kOffQ + qs * kQBytes;
+    const uint32_t qb = c.sbase + kOffQ + qs * S::kQBytes;
     // c_kv channels: 128-byte swizzle, 8-row groups 1 KB apart; k_pe
     // channels: 64-byte swizzle, 8-row groups 512 B apart
     const uint64_t a128 = smem_desc(stage, 16, 1024, kSwizzle128B);
     const uint64_t b128 = smem_desc(qb, 16, 1024, kSwizzle128B);
     const uint64_t a64 = smem_desc(stage + 4 * kBlk, 16, 512, kSwizzle64B);
-    const uint64_t b64 = smem_desc(qb + 4 * kQBlk, 16, 512, kSwizzle64B);
-    const uint32_t d = c.tmem + kColS + 32 * slot;
+    const uint64_t b64 = smem_desc(qb + 4 * S::kQBlk, 16, 512, kSwizzle64B);
+    const uint32_t d = c.tmem + kColS + S::kN * slot;
 #pragma unroll
     for (int ks = 0; ks < kKSteps; ++ks) {
         const uint64_t a = ks < 16 ? desc_at(a128, (ks >> 2) * kBlk + (ks & 3) * 32)
                                    : desc_at(a64, (ks - 16) * 32);
-        const uint64_t b = ks < 16 ? desc_at(b128, (ks >> 2) * kQBlk + (ks & 3) * 32)
+        const uint64_t b = ks < 16 ? desc_at(b128, (ks >> 2) * S::kQBlk + (ks & 3) * 32)
                                    : desc_at(b64, (ks - 16) * 32);
         mma_e4m3(d, a, b, c.idesc_qk, ks > 0);
     }
@@ -339,18 +362,21 @@ __device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
 }
 
 // PV of tile j into O buffer `ob`; the segment's first tile overwrites it.
+template <int G>
 __device__ __forceinline__ void issue_pv(const MmaCtx& c, int j, int ob, bool first) {
+    using S = Shape<G>;
     const int kv = j % kStages;
     // A = V^T: 128 channels (one column block) x 32 tokens, MN-major;
-    // B = [P1;P2]^T: 32 tokens x 32 (term, head), MN-major, unswizzled
+    // B = [P1;P2]^T: 32 tokens x kN (term, head), MN-major, unswizzled, one
+    // 16-column group (16 heads of one term) every kPUnit bytes
     const uint64_t a0 = smem_desc(c.sbase + kOffStage + kv * kStage, kBlk, 1024, kSwizzle128B);
-    const uint64_t b0 = smem_desc(c.sbase + kOffP + (j & 1) * kPBytes, 128, kPUnit, kSwizzleNone);
-    const uint32_t d = c.tmem + kColO + 128 * ob;
+    const uint64_t b0 = smem_desc(c.sbase + kOffP + (j & 1) * S::kPBytes, 128, kPUnit, kSwizzleNone);
+    const uint32_t d = c.tmem + S::kColO + 4 * S::kN * ob;
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
         for (int ks = 0; ks < kTT / 32; ++ks)
-            mma_e4m3(d + 32 * mb, desc_at(a0, mb * kBlk + ks * 32 * 128), desc_at(b0, ks * 32 * 16),
+            mma_e4m3(d + S::kN * mb, desc_at(a0, mb * kBlk + ks * 32 * 128), desc_at(b0, ks * 32 * 16),
                      c.idesc_pv, ks > 0 || !first);
     }
     mma_commit(&c.bars[PV_DONE + (j & 1)]);
@@ -383,7 +409,9 @@ struct SegWalk {
 // PV of tile i queued behind QK^T of tile i + 1 (and freed its stage late);
 // with two, each goes out as soon as its inputs are ready.  QK^T needs its
 // stage full, so it runs at most a stage ahead of PV by construction.
+template <int G>
 __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
+    using S = Shape<G>;
     int total = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
@@ -394,8 +422,9 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
     wq.init(p, seg_lo, seg_hi);
     for (int qk = 0; qk < total; ++qk) {
         const int slot = qk & 1;
-        const int qs = wq.k & 1;
-        if (wq.it == 0 && !mbar_wait(&c.bars[Q_FULL + qs], (static_cast<uint32_t>(wq.k) >> 1) & 1, c.abort, c.flags))
+        const int qs = wq.k % S::kQBufs;
+        if (wq.it == 0 &&
+            !mbar_wait(&c.bars[Q_FULL + qs], static_cast<uint32_t>(wq.k / S::kQBufs) & 1, c.abort, c.flags))
             break;
         if (!mbar_wait(&c.bars[KV_FULL + qk % kStages], static_cast<uint32_t>(qk / kStages) & 1, c.abort, c.flags))
             break;
@@ -403,7 +432,7 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
             break;
         fence_after_sync();
         fence_proxy_async_smem();
-        issue_qk(c, qk, qs);
+        issue_qk<G>(c, qk, qs);
         if (wq.it == wq.sg.ntiles - 1) mma_commit(&c.bars[Q_FREE + qs]);   // q buffer done
         wq.advance(p);
     }
@@ -413,20 +442,23 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
     mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
 }
 
+template <int G>
 __device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
+    using S = Shape<G>;
     const int total = count_tiles(p, seg_lo, seg_hi);
     SegWalk wp;
     wp.init(p, seg_lo, seg_hi);
     for (int pv = 0; pv < total; ++pv) {
-        const int ob = wp.k & 1;
+        const int ob = wp.k % S::kOBufs;
         if (!mbar_wait(&c.bars[P_FULL + (pv & 1)], (static_cast<uint32_t>(pv) >> 1) & 1, c.abort, c.flags)) break;
-        // a segment's first PV overwrites O buffer k & 1: segment k - 2 has been read out
+        // a segment's first PV overwrites its O buffer: the segment that used
+        // it before has been read out
         if (wp.it == 0 &&
-            !mbar_wait(&c.bars[O_FREE + ob], ((static_cast<uint32_t>(wp.k) >> 1) & 1) ^ 1, c.abort, c.flags))
+            !mbar_wait(&c.bars[O_FREE + ob], (static_cast<uint32_t>(wp.k / S::kOBufs) & 1) ^ 1, c.abort, c.flags))
             break;
         fence_after_sync();
         fence_proxy_async_smem();
-        issue_pv(c, pv, ob, wp.it == 0);
+        issue_pv<G>(c, pv, ob, wp.it == 0);
         wp.advance(p);
     }
     mma_commit(&c.bars[DONE]);
@@ -479,13 +511,15 @@ __device__ __forceinline__ float amax_bf16x8(const uint4& v, float a) {
 constexpr int kSplitThreads = 64;
 
 // One warp per (request, head row): lane c splits 16-channel chunk c of c_kv,
-// lanes 0-3 also chunk c of k_pe.  Heads are taken in groups of 16, one image
+// lanes 0-3 also chunk c of k_pe.  Heads are taken in groups of G, one image
 // per (request, group); heads >= H get zero rows and multiplier 0.
+template <int G>
 __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const DecodeParams p) {
+    using S = Shape<G>;
     griddep_launch_dependents();                // the decode kernel may start loading KV now
     const int wg = (blockIdx.x * kSplitThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int rows = p.head_groups * kHeadsPerCta;
-    const int b = wg / rows, head = wg % rows, r = head % kHeadsPerCta;
+    const int rows = p.head_groups * G;
+    const int b = wg / rows, head = wg % rows, r = head % G;
     if (b >= p.batch) return;
     const bool valid = head < p.heads;
     const uint4* src =
@@ -502,50 +536,51 @@ __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const Decode
     int sigma = amax > 0.f ? 8 - e2 : 0;            // max |q| * 2^sigma in [128, 256)
     sigma = sigma > 100 ? 100 : (sigma < -100 ? -100 : sigma);
     const float scale = ldexpf(1.f, sigma);
-    uint8_t* img = p.qimg + (int64_t(b) * p.head_groups + head / kHeadsPerCta) * kTcQImageBytes;
-    const int row1 = r, row2 = kHeadsPerCta + r;
+    uint8_t* img = p.qimg + (int64_t(b) * p.head_groups + head / G) * S::kImage;
+    const int row1 = r, row2 = G + r;
     uint4 t1, t2;
     split_chunk(va, vb, scale, t1, t2);
     {                                               // c_kv: 128-byte rows, 128-byte swizzle
         const int cb = lane >> 3, cc = lane & 7;
-        *reinterpret_cast<uint4*>(img + cb * kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4)) = t1;
-        *reinterpret_cast<uint4*>(img + cb * kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4)) = t2;
+        *reinterpret_cast<uint4*>(img + cb * S::kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4)) = t1;
+        *reinterpret_cast<uint4*>(img + cb * S::kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4)) = t2;
     }
     if (rope) {                                     // k_pe: 64-byte rows, 64-byte swizzle
         split_chunk(ra, rb, scale, t1, t2);
-        *reinterpret_cast<uint4*>(img + 4 * kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4)) = t1;
-        *reinterpret_cast<uint4*>(img + 4 * kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4)) = t2;
+        *reinterpret_cast<uint4*>(img + 4 * S::kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4)) = t1;
+        *reinterpret_cast<uint4*>(img + 4 * S::kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4)) = t2;
     }
     if (lane == 0)
-        reinterpret_cast<float*>(img + kQBytes)[r] =
+        reinterpret_cast<float*>(img + S::kQBytes)[r] =
             valid ? ldexpf(p.softmax_scale * p.k_scale * kLog2e, -sigma) : 0.f;
 }
-static_assert(kTcQImageBytes == kQBytes + kHeadsPerCta * 4, "q image = smem q buffer + multipliers");
 
-// Warp 5: fetches each segment's q image into q buffer k & 1 (and its
+// Warp 5: fetches each segment's q image into its q buffer (and the
 // multipliers) once the split kernel has finished.
+template <int G>
 __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                         int seg_lo, int seg_hi, int lane) {
+    using S = Shape<G>;
     if (lane != 0) return;
     griddep_wait();                                 // the q images are complete
     int k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
         if (sg.ntiles == 0) continue;
-        const int qs = k & 1;
-        const uint32_t qu = static_cast<uint32_t>(k) >> 1;
+        const int qs = k % S::kQBufs;
+        const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
         if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
-        const uint8_t* img = p.qimg + (int64_t(sg.b) * p.head_groups + blockIdx.y) * kTcQImageBytes;
-        mbar_arrive_expect_tx(&bars[Q_FULL + qs], kTcQImageBytes);
-        bulk_copy_g2s(smem_u32(base + kOffQ + qs * kQBytes), img, kQBytes, &bars[Q_FULL + qs]);
-        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * kHeadsPerCta * 4), img + kQBytes, kHeadsPerCta * 4,
-                      &bars[Q_FULL + qs]);
+        const uint8_t* img = p.qimg + (int64_t(sg.b) * p.head_groups + blockIdx.y) * S::kImage;
+        mbar_arrive_expect_tx(&bars[Q_FULL + qs], S::kImage);
+        bulk_copy_g2s(smem_u32(base + kOffQ + qs * S::kQBytes), img, S::kQBytes, &bars[Q_FULL + qs]);
+        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * G * 4), img + S::kQBytes, G * 4, &bars[Q_FULL + qs]);
         ++k;
     }
     // copies in flight (after an abort) land before the CTA exits
     volatile int never = 0;
-    for (int j = k - 2 < 0 ? 0 : k - 2; j < k; ++j)
-        mbar_wait(&bars[Q_FULL + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, &never, p.flags, 1000000000ull);
+    for (int j = k - S::kQBufs < 0 ? 0 : k - S::kQBufs; j < k; ++j)
+        mbar_wait(&bars[Q_FULL + j % S::kQBufs], static_cast<uint32_t>(j / S::kQBufs) & 1, &never, p.flags,
+                  1000000000ull);
 }
 
 // ------------------------------------------------- softmax / rescale WG
@@ -558,50 +593,76 @@ struct WgCtx {
     uint32_t* flags;
     int row;                // TMEM lane of O = channel within a 128-channel block
     int srow;               // token of S (M = 64: lanes 0-15 of each lane quadrant)
-    int hb;                 // heads hb .. hb+7 of token srow are this lane's: lanes 0-15
-                            // take heads 0-7 and lanes 16-31 heads 8-15 of the same tokens
+    int hb;                 // heads hb .. hb + G/2 - 1 of token srow are this lane's: lanes
+                            // 0-15 take the first half of the heads, 16-31 the second
     int wq, lane;           // softmax warp 0..3, lane
 };
 
-// O (one segment's accumulator) *= alpha per head, in TMEM.  Columns h and
-// 16 + h of each 128-channel block hold head h's two P terms.
-__device__ __forceinline__ void rescale_o(const WgCtx& w, uint32_t ocol, const float (&alpha)[16]) {
+// O (one segment's accumulator) *= alpha per head, in TMEM.  Each
+// 128-channel block holds kN columns: head h's two P terms in columns h and
+// G + h.
+template <int G>
+__device__ __forceinline__ void rescale_o(const WgCtx& w, uint32_t ocol, const float (&alpha)[G]) {
+    using S = Shape<G>;
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
-        uint32_t r1[16], r2[16];
-        tmem_ld16(w.tmem_lane + ocol + 32 * mb, r1);
-        tmem_ld16(w.tmem_lane + ocol + 32 * mb + 16, r2);
-        tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-            r1[h] = __float_as_uint(__uint_as_float(r1[h]) * alpha[h]);
-            r2[h] = __float_as_uint(__uint_as_float(r2[h]) * alpha[h]);
+        for (int c = 0; c < S::kN / 16; c += 2) {         // two loads in flight per wait
+            uint32_t r[2][16];
+            tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c, r[0]);
+            tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c + 16, r[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    r[cc][i] = __float_as_uint(__uint_as_float(r[cc][i]) * alpha[(16 * (c + cc)) % G + i]);
+                tmem_st16(w.tmem_lane + ocol + S::kN * mb + 16 * (c + cc), r[cc]);
+            }
         }
-        tmem_st16(w.tmem_lane + ocol + 32 * mb, r1);
-        tmem_st16(w.tmem_lane + ocol + 32 * mb + 16, r2);
     }
     tmem_wait_st();
 }
 
-// Reduction over the 16 lanes of a half warp of 8 values at once by halving
-// exchanges (8 shuffles instead of 32): afterwards lane l holds value
-// (l >> 1) & 7 reduced over its half.
-template <bool kMax>
-__device__ __forceinline__ float half_reduce8(const float (&v)[8], int lane) {
+// Reduction over the 16 lanes of a half warp of V (8 or 16) values at once by
+// halving exchanges (V shuffles instead of 4 V): afterwards lane l holds
+// value idx(l) reduced over its half, idx = (l >> 1) & 7 for V = 8 (lanes l
+// and l ^ 1 agree) and l & 15 for V = 16.
+template <bool kMax, int V>
+__device__ __forceinline__ float half_reduce(const float (&v)[V], int lane) {
     auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-    float a4[4], a2[2];
-    const bool b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+    float a8[8], a4[4], a2[2];
+    if constexpr (V == 16) {
+        const bool b3 = lane & 8;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            a8[j] = op(b3 ? v[j + 8] : v[j], __shfl_xor_sync(0xffffffffu, b3 ? v[j] : v[j + 8], 8));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a8[j] = v[j];
+    }
+    const int s4 = V == 16 ? 4 : 8, s2 = V == 16 ? 2 : 4, s1 = V == 16 ? 1 : 2;
+    const bool c4 = lane & s4, c2 = lane & s2, c1 = lane & s1;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-        a4[j] = op(b3 ? v[j + 4] : v[j], __shfl_xor_sync(0xffffffffu, b3 ? v[j] : v[j + 4], 8));
+        a4[j] = op(c4 ? a8[j + 4] : a8[j], __shfl_xor_sync(0xffffffffu, c4 ? a8[j] : a8[j + 4], s4));
 #pragma unroll
     for (int j = 0; j < 2; ++j)
-        a2[j] = op(b2 ? a4[j + 2] : a4[j], __shfl_xor_sync(0xffffffffu, b2 ? a4[j] : a4[j + 2], 4));
-    const float a1 = op(b1 ? a2[1] : a2[0], __shfl_xor_sync(0xffffffffu, b1 ? a2[0] : a2[1], 2));
-    return op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
+        a2[j] = op(c2 ? a4[j + 2] : a4[j], __shfl_xor_sync(0xffffffffu, c2 ? a4[j] : a4[j + 2], s2));
+    const float a1 = op(c1 ? a2[1] : a2[0], __shfl_xor_sync(0xffffffffu, c1 ? a2[0] : a2[1], s1));
+    return V == 16 ? a1 : op(a1, __shfl_xor_sync(0xffffffffu, a1, 1));
 }
 
+template <int V>
+__device__ __forceinline__ int half_reduce_index(int lane) { return V == 16 ? (lane & 15) : ((lane >> 1) & 7); }
+
+template <int V>
+__device__ __forceinline__ bool half_reduce_writer(int lane) { return V == 16 || (lane & 1) == 0; }
+
+template <int G>
 __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, int seg_hi, int head0) {
+    using S = Shape<G>;
+    constexpr int kHL = S::kHL;
     float* red = reinterpret_cast<float*>(w.base + kOffRed);
     float* lsum = reinterpret_cast<float*>(w.base + kOffLsum);
     int* vote = reinterpret_cast<int*>(w.base + kOffFlag);
@@ -615,17 +676,17 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
     for (int si = seg_lo; si < seg_hi; ++si) {
         const Seg sg = load_seg(p, si);
         if (sg.ntiles == 0) continue;
-        const int qs = k & 1;
-        const uint32_t qu = static_cast<uint32_t>(k) >> 1;
-        const uint32_t ocol = kColO + 128 * (k & 1);
+        const int qs = k % S::kQBufs;
+        const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
+        const uint32_t ocol = S::kColO + 4 * S::kN * (k % S::kOBufs);
         mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags);
-        // the segment's score multipliers stay in shared memory (q buffer qs
+        // the segment's score multipliers stay in shared memory (its q buffer
         // is released at the end of the segment)
-        const float* coef = coefs + qs * kHeadsPerCta;
+        const float* coef = coefs + qs * G;
 
-        float m[8], l[8];                           // heads hb .. hb+7
+        float m[kHL], l[kHL];                       // heads hb .. hb + kHL - 1
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < kHL; ++j) {
             m[j] = -INFINITY;
             l[j] = 0.f;
         }
@@ -640,21 +701,32 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
             mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
             fence_after_sync();
-            uint32_t r1[16], r2[16];
-            tmem_ld16(w.tmem_lane + kColS + 32 * slot, r1);
-            tmem_ld16(w.tmem_lane + kColS + 32 * slot + 16, r2);
-            tmem_wait_ld();
+            // lanes 0-15 hold the token's G heads: column h (q1 term) + G + h (q2)
+            float sum[G];
+#pragma unroll
+            for (int c = 0; c < S::kN / 16; c += 2) {     // two loads in flight per wait
+                uint32_t r[2][16];
+                tmem_ld16(w.tmem_lane + kColS + S::kN * slot + 16 * c, r[0]);
+                tmem_ld16(w.tmem_lane + kColS + S::kN * slot + 16 * c + 16, r[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int h = (16 * (c + cc)) % G + t;
+                        sum[h] = 16 * (c + cc) < G ? __uint_as_float(r[cc][t]) : sum[h] + __uint_as_float(r[cc][t]);
+                    }
+            }
             fence_before_sync();
             mbar_arrive(&w.bars[S_FREE + slot]);
 
-            // lanes 0-15 hold the token's 16 heads; heads 8-15 move to lanes 16-31
-            float s[8];
+            // the second half of the heads moves to lanes 16-31
+            float s[kHL];
             bool need = false;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float hi = __shfl_sync(0xffffffffu, __uint_as_float(r1[8 + j]) + __uint_as_float(r2[8 + j]),
-                                             w.lane & 15);
-                const float raw = w.hb ? hi : __uint_as_float(r1[j]) + __uint_as_float(r2[j]);
+            for (int j = 0; j < kHL; ++j) {
+                const float hi = __shfl_sync(0xffffffffu, sum[kHL + j], w.lane & 15);
+                const float raw = w.hb ? hi : sum[j];
                 s[j] = valid ? raw * coef[w.hb + j] : -INFINITY;
                 need |= s[j] > m[j] + kTau;         // always true on a segment's first tile
             }
@@ -666,15 +738,15 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             wg_bar();
             need = vb[0] | vb[1] | vb[2] | vb[3];
             if (need) {
-                const float hmax = half_reduce8<true>(s, w.lane);
-                float* rb = red + (i & 1) * 64;
-                if ((w.lane & 1) == 0) rb[w.wq * 16 + w.hb + ((w.lane >> 1) & 7)] = hmax;
+                const float hmax = half_reduce<true, kHL>(s, w.lane);
+                float* rb = red + (i & 1) * 4 * G;
+                if (half_reduce_writer<kHL>(w.lane)) rb[w.wq * G + w.hb + half_reduce_index<kHL>(w.lane)] = hmax;
                 wg_bar();
-                float alpha[8];
+                float alpha[kHL];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < kHL; ++j) {
                     const int h = w.hb + j;
-                    const float tmax = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
+                    const float tmax = fmaxf(fmaxf(rb[h], rb[G + h]), fmaxf(rb[2 * G + h], rb[3 * G + h]));
                     const float mn = fmaxf(m[j], tmax);
                     alpha[j] = m[j] == -INFINITY ? 0.f : fast_exp2(m[j] - mn);
                     m[j] = mn;
@@ -682,25 +754,25 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                 }
                 if (it > 0) {
                     // O holds tiles up to i - 1: rescale once PV(i - 1) has landed;
-                    // every lane needs all 16 heads' factors (lanes 0 and 16 have them)
-                    float a16[16];
+                    // every lane needs all G heads' factors (lanes 0 and 16 have them)
+                    float a_all[G];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        a16[j] = __shfl_sync(0xffffffffu, alpha[j], 0);
-                        a16[8 + j] = __shfl_sync(0xffffffffu, alpha[j], 16);
+                    for (int j = 0; j < kHL; ++j) {
+                        a_all[j] = __shfl_sync(0xffffffffu, alpha[j], 0);
+                        a_all[kHL + j] = __shfl_sync(0xffffffffu, alpha[j], 16);
                     }
                     const int j = i - 1;
                     mbar_wait(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort, w.flags);
                     fence_after_sync();
-                    rescale_o(w, ocol, a16);
+                    rescale_o<G>(w, ocol, a_all);
                 }
             }
             // P = 2^(s - m) <= 2^kTau, stored as two E4M3 terms of p * kPScale;
             // its buffer was last read by PV(i - 2)
             if (i >= 2) mbar_wait(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags);
-            uint32_t pk1[2], pk2[2];
+            uint32_t pk1[kHL / 4], pk2[kHL / 4];
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
+            for (int e2 = 0; e2 < kHL / 4; ++e2) {
                 uint32_t w1 = 0, w2 = 0;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
@@ -719,9 +791,16 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                 pk1[e2] = w1;
                 pk2[e2] = w2;
             }
-            uint8_t* pb = pbase + slot * kPBytes + w.srow * 16 + w.hb;
-            *reinterpret_cast<uint2*>(pb) = make_uint2(pk1[0], pk1[1]);
-            *reinterpret_cast<uint2*>(pb + kPUnit) = make_uint2(pk2[0], pk2[1]);
+            // [P1;P2]^T: 16-head column group g = term * (G / 16) + head / 16
+            uint8_t* pb = pbase + slot * S::kPBytes + (w.hb / 16) * kPUnit + w.srow * 16 + (w.hb % 16);
+            uint8_t* pb2 = pb + (G / 16) * kPUnit;
+            if constexpr (kHL == 8) {
+                *reinterpret_cast<uint2*>(pb) = make_uint2(pk1[0], pk1[1]);
+                *reinterpret_cast<uint2*>(pb2) = make_uint2(pk2[0], pk2[1]);
+            } else {
+                *reinterpret_cast<uint4*>(pb) = make_uint4(pk1[0], pk1[1], pk1[2], pk1[3]);
+                *reinterpret_cast<uint4*>(pb2) = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
+            }
             fence_proxy_async_smem();
             fence_before_sync();                    // orders a rescale's TMEM stores too
             mbar_arrive(&w.bars[P_FULL + slot]);
@@ -729,16 +808,23 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
 
         // ---- epilogue: denominators over the token lanes, normalise, store
         {
-            const float hsum = half_reduce8<false>(l, w.lane);
-            if ((w.lane & 1) == 0) lsum[w.wq * 16 + w.hb + ((w.lane >> 1) & 7)] = hsum;
+            const float hsum = half_reduce<false, kHL>(l, w.lane);
+            if (half_reduce_writer<kHL>(w.lane)) lsum[w.wq * G + w.hb + half_reduce_index<kHL>(w.lane)] = hsum;
         }
         wg_bar();
-        float inv[16], L[16];
+        float inv[G];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) L[h] = lsum[h] + lsum[16 + h] + lsum[32 + h] + lsum[48 + h];
+        for (int h = 0; h < G; ++h) {
+            const float L = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
+            inv[h] = L > 0.f ? p.k_scale / L : 0.f;
+        }
+        float Lmine[kHL];                           // this lane's heads, for the lse
+#pragma unroll
+        for (int j = 0; j < kHL; ++j) {
+            const int h = w.hb + j;
+            Lmine[j] = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
+        }
         wg_bar();                                   // lsum is reused by the next segment
-#pragma unroll
-        for (int h = 0; h < 16; ++h) inv[h] = L[h] > 0.f ? p.k_scale / L[h] : 0.f;
         const int jl = i - 1;                       // the segment's last tile
         mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
@@ -747,43 +833,54 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         const float lse_off = -kTau;                 // kPScale = 2^kTau
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
-            uint32_t r1[16], r2[16];
-            tmem_ld16(w.tmem_lane + ocol + 32 * mb, r1);
-            tmem_ld16(w.tmem_lane + ocol + 32 * mb + 16, r2);
-            tmem_wait_ld();
+            float o[G];
+#pragma unroll
+            for (int c = 0; c < S::kN / 16; c += 2) {     // two loads in flight per wait
+                uint32_t r[2][16];
+                tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c, r[0]);
+                tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c + 16, r[1]);
+                tmem_wait_ld();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int h = (16 * (c + cc)) % G + t;
+                        o[h] = 16 * (c + cc) < G ? __uint_as_float(r[cc][t]) : o[h] + __uint_as_float(r[cc][t]);
+                    }
+            }
             const int ch = mb * 128 + w.row;
             if (sg.part < 0) {
                 uint16_t* out = p.out + (int64_t(sg.b) * H + head0) * kDCkv + ch;
 #pragma unroll
-                for (int h = 0; h < 16; ++h) {
+                for (int h = 0; h < G; ++h) {
                     if (head0 + h >= H) break;
-                    const float o = __uint_as_float(r1[h]) + __uint_as_float(r2[h]);
-                    out[h * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o * inv[h]));
+                    out[h * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h] * inv[h]));
                 }
             } else {
                 float* po = p.part_o + (int64_t(sg.part) * H + head0) * kDCkv + ch;
 #pragma unroll
-                for (int h = 0; h < 16; ++h) {
+                for (int h = 0; h < G; ++h) {
                     if (head0 + h >= H) break;
-                    po[h * kDCkv] = (__uint_as_float(r1[h]) + __uint_as_float(r2[h])) * inv[h];
+                    po[h * kDCkv] = o[h] * inv[h];
                 }
             }
         }
         fence_before_sync();
-        mbar_arrive(&w.bars[O_FREE + (k & 1)]);      // the next segment but one may overwrite O
+        mbar_arrive(&w.bars[O_FREE + (k % S::kOBufs)]);   // a later segment may overwrite O
         mbar_arrive(&w.bars[Q_FREE + qs]);
-        if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb+7
+        if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb + kHL - 1
             float* dst = sg.part < 0 ? p.lse + int64_t(sg.b) * H : p.part_lse + int64_t(sg.part) * H;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                if (head0 + w.hb + j < H)
-                    dst[head0 + w.hb + j] = (m[j] + log2f(w.hb ? L[8 + j] : L[j]) + lse_off) * kLn2;
+            for (int j = 0; j < kHL; ++j)
+                if (head0 + w.hb + j < H) dst[head0 + w.hb + j] = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
         }
         ++k;
     }
 }
 
+template <int G>
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const DecodeParams p) {
+    using S = Shape<G>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBar);
@@ -811,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int seg_lo = p.cta_ptr[blockIdx.x], seg_hi = p.cta_ptr[blockIdx.x + 1];
-    const int head0 = blockIdx.y * kHeadsPerCta;  // heads head0 .. head0 + 15 of every request
+    const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == kWarpSched) {
         scheduler(p, base, bars, abort, seg_lo, seg_hi, lane);
@@ -822,17 +919,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
             MmaCtx c;
             c.sbase = smem_u32(base);
             c.tmem = tmem;
-            c.idesc_qk = idesc_e4m3_f32(kTT, 32, false, false);
-            c.idesc_pv = idesc_e4m3_f32(128, 32, true, true);   // M = 128 channels of a block
+            c.idesc_qk = idesc_e4m3_f32(kTT, S::kN, false, false);
+            c.idesc_pv = idesc_e4m3_f32(128, S::kN, true, true);   // M = 128 channels of a block
             c.bars = bars;
             c.abort = abort;
             c.flags = p.flags;
-            if (warp == kWarpMma) qk_issuer(p, c, seg_lo, seg_hi);
-            else pv_issuer(p, c, seg_lo, seg_hi);
+            if (warp == kWarpMma) qk_issuer<G>(p, c, seg_lo, seg_hi);
+            else pv_issuer<G>(p, c, seg_lo, seg_hi);
         }
         __syncwarp();
     } else if (warp == kWarpQ) {
-        q_fetch(p, base, bars, abort, seg_lo, seg_hi, lane);
+        q_fetch<G>(p, base, bars, abort, seg_lo, seg_hi, lane);
     } else {                                      // warps kWarpWg .. kWarpWg + 3
         WgCtx w;
         w.base = base;
@@ -843,10 +940,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
         w.flags = p.flags;
         w.row = quad * 32 + lane;
         w.srow = quad * 16 + (lane & 15);
-        w.hb = (lane >> 4) * 8;
+        w.hb = (lane >> 4) * S::kHL;
         w.wq = warp - kWarpWg;
         w.lane = lane;
-        softmax_wg(p, w, seg_lo, seg_hi, head0);
+        softmax_wg<G>(p, w, seg_lo, seg_hi, head0);
     }
     fence_before_sync();
     __syncthreads();
@@ -858,34 +955,28 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
 }
 
 std::mutex g_mu;
-std::vector<char> g_attr;     // per device: max dynamic smem set
+std::vector<char> g_attr;     // per device: bit 0 / 1: max dynamic smem set for G = 16 / 32
 
-}  // namespace
-
-cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+template <int G>
+cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int dev) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if ((int)g_attr.size() <= dev) g_attr.resize(dev + 1, 0);
-        if (!g_attr[dev]) {
-            e = cudaFuncSetAttribute(mla_decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemBytes);
+        const char bit = G == 16 ? 1 : 2;
+        if (!(g_attr[dev] & bit)) {
+            const cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<G>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
-            g_attr[dev] = 1;
+            g_attr[dev] |= bit;
         }
     }
-    // slots are held as int32 in the kernel's shared slot lists
-    if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
-    const int split_blocks =
-        (p.batch * p.head_groups * kHeadsPerCta * 32 + kSplitThreads - 1) / kSplitThreads;
-    mla_q_split_kernel<<<split_blocks, kSplitThreads, 0, stream>>>(p);
-    e = cudaGetLastError();
+    const int split_blocks = (p.batch * p.head_groups * G * 32 + kSplitThreads - 1) / kSplitThreads;
+    mla_q_split_kernel<G><<<split_blocks, kSplitThreads, 0, stream>>>(p);
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the decode kernel starts while the split runs: only its q warp waits
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid, p.head_groups);         // token ranges x 16-head groups
+    cfg.gridDim = dim3(grid, p.head_groups);         // token ranges x head groups
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -894,7 +985,20 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel, p);
+    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    // slots are held as int32 in the kernel's shared slot lists
+    if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
+    if (p.group_heads == 32) return launch_g<32>(p, grid, stream, dev);
+    if (p.group_heads == 16) return launch_g<16>(p, grid, stream, dev);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace mla

@@ -136,7 +136,10 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
     s.kernel = kernel;
     s.tile_tokens = static_cast<int32_t>(tile);
     s.n_tokens = n_tokens;
-    s.head_groups = (H + kHeadsPerCta - 1) / kHeadsPerCta;
+    // the tcgen05 kernel takes 32 heads per CTA when it can: one read of a tile
+    // then serves twice the heads
+    s.group_heads = (kernel == DecodeKernel::kTc && H % 32 == 0) ? 32 : kHeadsPerCta;
+    s.head_groups = (H + s.group_heads - 1) / s.group_heads;
 
     int64_t ctas = static_cast<int64_t>(num_sms) * ctas_per_sm(kernel) / s.head_groups;
     if (ctas < 1) ctas = 1;
@@ -194,7 +197,8 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
     if (kernel == DecodeKernel::kTc && s.num_ctas > 0) {
         s.qimg_offset = s.workspace_bytes;
         s.workspace_bytes =
-            align256(s.qimg_offset + static_cast<size_t>(B) * s.head_groups * kTcQImageBytes);
+            align256(s.qimg_offset + static_cast<size_t>(B) * s.head_groups * (s.group_heads / 16) *
+                                         kTcQImageBytes);
     }
     return MLA_OK;
 }

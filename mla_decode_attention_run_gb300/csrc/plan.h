@@ -40,7 +40,8 @@ struct Schedule {
     mla_kv_dtype_t kv_dtype = MLA_KV_FP8_E4M3;
     DecodeKernel kernel = DecodeKernel::kMma;
     int32_t tile_tokens = kTileTokens;
-    int32_t head_groups = 0;
+    int32_t head_groups = 0;         // CTAs per token range (grid.y)
+    int32_t group_heads = 16;        // heads per CTA: 16, or 32 on the tcgen05 path when H % 32 == 0
     int32_t num_ctas = 0;            // token ranges; grid = num_ctas * head_groups
     std::vector<int32_t> cta_ptr;    // [num_ctas + 1] -> segment index
     std::vector<int32_t> segs;       // 4 per segment: request, t0, t1, partial (-1 = final)

@@ -76,7 +76,8 @@ def _check_schedule(segs, info, lens, heads, num_sms=152):
     parts = segs[segs[:, 4] >= 0, 4]
     assert np.array_equal(np.sort(parts), np.arange(info["num_partials"]))
     ctas = info["num_ctas"]
-    hg = (heads + 15) // 16
+    # CTAs per token range: 32 heads each on the tcgen05 path when they divide H, else 16
+    hg = heads // 32 if (tc and heads % 32 == 0) else (heads + 15) // 16
     assert ctas <= max(1, num_sms // hg)
     tiles = np.zeros(ctas, np.int64)
     cost = np.zeros(ctas, np.int64)
@@ -97,7 +98,7 @@ def _check_schedule(segs, info, lens, heads, num_sms=152):
     ws = info["workspace_bytes"]
     need = info["num_partials"] * heads * (512 + 1) * 4
     if tc and ctas > 0:                    # tcgen05 path: one q image per request and head group
-        need += len(lens) * hg * QIMAGE_BYTES
+        need += len(lens) * ((heads + 15) // 16) * QIMAGE_BYTES
     assert ws >= need
     if need == 0:
         assert ws == 0
@@ -119,7 +120,7 @@ def test_schedule_large_head_paged():
     lens = np.full(128, 32768)
     segs, info = M.mla_decode_schedule(_indptr(lens, 64), lens, 128, 128, 64)
     _check_schedule(segs, info, lens, 128)
-    assert info["num_ctas"] == 152 // 8
+    assert info["num_ctas"] == 152 // 4          # 32-head CTAs: four per token range
 
 
 def test_schedule_ragged_and_empty_requests():
