@@ -64,6 +64,9 @@ def _load():
         lib.oracle_decode_fp8.restype = ctypes.c_int
         lib.oracle_decode_bf16.argtypes = dec_args
         lib.oracle_decode_bf16.restype = ctypes.c_int
+        lib.oracle_extend_fp8.argtypes = [P, P, i64, P, i64, i64, P, P, P, P, i32, i32, i32,
+                                          f64, f64, P, P, ctypes.c_int]
+        lib.oracle_extend_fp8.restype = ctypes.c_int
         lib.oracle_attention_f64.argtypes = [P, P, i64, i32, f64, P, P, P]
         lib.oracle_max_threads.restype = ctypes.c_int
         _lib = lib
@@ -182,6 +185,36 @@ def decode_bf16(q_bf16, ckv_pool, kpe_pool, kv_indptr, kv_indices, seq_lens, pag
     """fp64 paged MLA decode over BF16 pools (uint16 [num_slots, stride])."""
     return _decode(_load().oracle_decode_bf16, q_bf16, ckv_pool, kpe_pool, kv_indptr,
                    kv_indices, seq_lens, page_size, k_scale, softmax_scale, want_p, nthreads)
+
+
+def extend_fp8(q_bf16, ckv_pool, kpe_pool, qo_indptr, kv_indptr, kv_indices, seq_lens,
+               page_size, k_scale, softmax_scale, nthreads=0):
+    """fp64 causal extend attention over E4M3 uint8 pools.
+
+    q_bf16: uint16 [n_q, H, 576], the new tokens of request b in rows
+    qo_indptr[b] .. qo_indptr[b+1]-1; seq_lens count the new tokens.  New
+    token i of request b sees the first seq_lens[b] - q_len_b + i + 1 tokens.
+    Returns o float64 [n_q, H, 512] and lse float64 [n_q, H] (natural log).
+    """
+    q = np.ascontiguousarray(q_bf16, np.uint16)
+    n_q, H, D = q.shape
+    assert D == D_ALL
+    qo = np.ascontiguousarray(qo_indptr, np.int32)
+    indptr = np.ascontiguousarray(kv_indptr, np.int32)
+    indices = np.ascontiguousarray(kv_indices, np.int32)
+    lens = np.ascontiguousarray(seq_lens, np.int32)
+    B = lens.shape[0]
+    assert qo.shape == (B + 1,) and indptr.shape == (B + 1,) and int(qo[-1]) == n_q
+    o = np.zeros((n_q, H, D_CKV), np.float64)
+    lse = np.zeros((n_q, H), np.float64)
+    rc = _load().oracle_extend_fp8(
+        _ptr(q), ckv_pool.ctypes.data, ckv_pool.strides[0], kpe_pool.ctypes.data,
+        kpe_pool.strides[0], ckv_pool.shape[0], _ptr(qo), _ptr(indptr), _ptr(indices),
+        _ptr(lens), B, H, int(page_size), float(k_scale), float(softmax_scale), _ptr(o),
+        _ptr(lse), int(nthreads))
+    if rc != 0:
+        raise IndexError("query lengths, page table or slots inconsistent with the contexts")
+    return o, lse
 
 
 def attention_f64(q: np.ndarray, k: np.ndarray, softmax_scale: float, want_p=False):

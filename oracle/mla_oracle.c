@@ -324,6 +324,80 @@ int oracle_decode_bf16(const uint16_t* q_bf16, const uint16_t* ckv_pool,
                          lse, p, p_stride, nthreads);
 }
 
+/* Causal extend (prefill with a cached prefix) over E4M3 pool rows.
+ *
+ * [P1] "Step 3: Source Validation", CastFromFP8: on every extend step the
+ * prefill attention reads the request's whole cached history, which the FP8
+ * configuration first casts back to BF16; "From Attribution to Optimization
+ * Targets" names the fix, a prefill attention that reads the FP8 cache
+ * itself.  The pages do not write the extend attention out; the reading used
+ * here is the usual causal one, in the same latent (576-channel query, 512-
+ * channel value) form as decode:
+ *  - request b has q_len_b = qo_indptr[b+1] - qo_indptr[b] new tokens, whose
+ *    query rows are rows qo_indptr[b] .. qo_indptr[b+1]-1 of q; they are
+ *    already in the cache (the store precedes attention), so its context
+ *    L_b = seq_lens[b] counts them, and 0 <= q_len_b <= L_b;
+ *  - new token i (0-based) sits at sequence position L_b - q_len_b + i and
+ *    attends to the tokens at positions 0 .. L_b - q_len_b + i, inclusive:
+ *    the decode attention above over the first L_b - q_len_b + i + 1 tokens.
+ * q: BF16 bits [n_q][H][576] (contiguous, n_q = qo_indptr[B]); o: [n_q][H][512];
+ * lse: [n_q][H].  Returns -1 when a q_len is negative or above its context,
+ * a page table is too short, or a slot is outside the pool; else 0. */
+int oracle_extend_fp8(const uint16_t* q_bf16, const uint8_t* ckv_pool,
+                      int64_t ckv_stride, const uint8_t* kpe_pool,
+                      int64_t kpe_stride, int64_t num_slots,
+                      const int32_t* qo_indptr, const int32_t* kv_indptr,
+                      const int32_t* kv_indices, const int32_t* seq_lens,
+                      int32_t B, int32_t H, int32_t page_size, double k_scale,
+                      double softmax_scale, double* o, double* lse, int nthreads) {
+    if (qo_indptr[0] != 0) return -1;
+    for (int32_t b = 0; b < B; ++b) {
+        int64_t L = seq_lens[b];
+        int64_t q_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        int64_t pages = kv_indptr[b + 1] - kv_indptr[b];
+        if (L < 0 || q_len < 0 || q_len > L || pages * page_size < L) return -1;
+        for (int64_t t = 0; t < L; ++t) {
+            int64_t s = token_slot(kv_indices + kv_indptr[b], t, page_size);
+            if (s < 0 || s >= num_slots) return -1;
+        }
+    }
+    const int64_t n_q = qo_indptr[B];
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+    (void)nthreads;
+#endif
+    /* one (query token, head) pair per iteration */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t nh = 0; nh < n_q * H; ++nh) {
+        int64_t n = nh / H;
+        int32_t h = (int32_t)(nh % H);
+        int32_t b = 0;
+        while (qo_indptr[b + 1] <= n) ++b;
+        int64_t q_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
+        int64_t i = n - qo_indptr[b];
+        int64_t visible = (int64_t)seq_lens[b] - q_len + i + 1;
+        const int32_t* pages = kv_indices + kv_indptr[b];
+        double qh[D_ALL];
+        for (int d = 0; d < D_ALL; ++d)
+            qh[d] = bf16_to_float(q_bf16[(n * H + h) * D_ALL + d]);
+        double* k = (double*)malloc(sizeof(double) * (size_t)visible * D_ALL);
+        double* s_buf = (double*)malloc(sizeof(double) * (size_t)visible);
+        for (int64_t t = 0; t < visible; ++t) {
+            int64_t slot = token_slot(pages, t, page_size);
+            for (int d = 0; d < D_CKV; ++d)
+                k[t * D_ALL + d] = pool_value(0, ckv_pool, ckv_stride, slot, d, k_scale);
+            for (int d = 0; d < D_KPE; ++d)
+                k[t * D_ALL + D_CKV + d] = pool_value(0, kpe_pool, kpe_stride, slot, d, k_scale);
+        }
+        attention_one_request(qh, k, visible, 1, softmax_scale, o + (n * H + h) * D_CKV,
+                              lse + n * H + h, NULL, s_buf);
+        free(k);
+        free(s_buf);
+    }
+    return 0;
+}
+
 /* The attention core alone, on explicit fp64 rows: q [H][576], k [L][576]. */
 void oracle_attention_f64(const double* q, const double* k, int64_t L, int32_t H,
                           double softmax_scale, double* o, double* lse, double* p) {
