@@ -393,6 +393,7 @@ def run_ours(args, rank, world, local):
     # ---- the other configurations' decode call, timed alone (rank 0)
     if rank == 0 and not args.no_configs:
         result["configs"] = measure_configs(torch, M, dev, stream)
+        result["extend"] = measure_extend(torch, M, dev, stream)
 
     # ---- CPU oracle baseline (rank 0, one GPU)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -465,6 +466,89 @@ def measure_configs(torch, M, dev, stream):
         M.mla_decode_plan_destroy(plan)
         del pool, q, out, lse, ws, g
         torch.cuda.empty_cache()
+    return res
+
+
+def measure_extend(torch, M, dev, stream, n_pools=8):
+    """Causal extend calls (several new tokens per request over a cached
+    history), each timed as a CUDA graph of calls rotating over n_pools
+    random E4M3 pools (one per layer; together larger than L2).  Beside each:
+    the gather-then-cast of the same pages, the least a BF16 prefill kernel
+    would need before it runs, which the FP8-native extend does not do."""
+    peak, _ = measured_peaks()
+    tflops_peak = None
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            tflops_peak = float(json.load(f).get("bf16_tflops", 0)) or None
+    res = {}
+    P = W.POOL_SLOTS
+    pools = torch.randint(0, 256, (n_pools, P, W.D_ALL), dtype=torch.uint8, device=dev)
+    pools[(pools & 0x7F) == 0x7F] = 0x3C
+    for name in ("spec_decode", "extend_chunk"):
+        w = W.make_extend_workload(name, latent_requests=[])
+        qo = w.extra["qo_indptr"]
+        q_lens = np.diff(qo)
+        B, H, ps, n_q = w.batch, w.heads, w.page_size, int(qo[-1])
+        q = torch.randn(n_pools, n_q, H, W.D_ALL, device=dev).to(torch.bfloat16)
+        out = torch.empty(n_pools, n_q, H, 512, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(n_pools, n_q, H, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            plan = M.mla_extend_plan(qo, w.kv_indptr, w.seq_lens, B, H, ps, stream=stream)
+        ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=dev)
+        ip, ix, ln = (torch.from_numpy(a).to(dev) for a in (w.kv_indptr, w.kv_indices, w.seq_lens))
+        rows = int(ix.numel()) * ps
+        ckv_c = torch.empty(rows, 512, dtype=torch.bfloat16, device=dev)
+        kpe_c = torch.empty(rows, 64, dtype=torch.bfloat16, device=dev)
+        info = M.mla_extend_schedule(qo, w.kv_indptr, w.seq_lens, B, H, ps)[2]
+
+        def extend(l, s):
+            M.mla_extend_run(plan, q[l], pools[l, :, :512], pools[l, :, 512:], P, ip, ix, ln,
+                             w.k_scale, W.SOFTMAX_SCALE, out[l], lse[l], ws, stream=s)
+
+        def gather(l, s):
+            M.kv_gather_cast(pools[l, :, :512], pools[l, :, 512:], ix, ps, 1.0, ckv_c, kpe_c,
+                             stream=s)
+
+        def time_graph(fn):
+            with torch.cuda.stream(stream):
+                for l in range(n_pools):
+                    fn(l, stream)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for l in range(n_pools):
+                    fn(l, torch.cuda.current_stream())
+            with torch.cuda.stream(stream):
+                g.replay()
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(3):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (3 * n_pools)
+
+        us = time_graph(extend)
+        us_cast = time_graph(gather)
+        nbytes = A.extend_call_bytes(w.seq_lens, q_lens, H, ps)
+        flops = A.extend_call_flops(w.seq_lens, q_lens, H)
+        r = {"batch": B, "heads": H, "page_size": ps, "new_tokens_per_request": int(q_lens[0]),
+             "context_tokens": int(w.seq_lens.sum()), "visible_tokens":
+             A.extend_visible_tokens(w.seq_lens, q_lens), "block_rows": info["block_rows"],
+             "blocks": info["num_blocks"], "us_per_call": round(us, 3),
+             "achieved_gbs": round(nbytes / us / 1e3, 1), "hbm_frac": round(nbytes / us / 1e3 / peak, 4),
+             "tflops": round(flops / us / 1e6, 2),
+             "gather_cast_us": round(us_cast, 3),
+             "gather_cast_note": "kv_gather_cast of the same pages to BF16 (not part of the FP8 extend)"}
+        if tflops_peak:
+            r["tensor_frac"] = round(flops / us / 1e6 / tflops_peak, 4)
+        res[name] = r
+        M.mla_decode_plan_destroy(plan)
+        del q, out, lse, ws, ckv_c, kpe_c
+    del pools
+    torch.cuda.empty_cache()
     return res
 
 

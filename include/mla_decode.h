@@ -94,8 +94,8 @@ typedef struct mla_plan* mla_plan_t;
  *                   + t % page_size.
  *  kv_dtype         element type of the pools run() will read.
  *  workspace_bytes  out: device scratch run() needs: the split-KV partials
- *                   and, on the tensor-core FP8 path (H <= 16), one
- *                   18,496-byte image of each request's split query.
+ *                   and, on the tensor-core FP8 path, one 18,560-byte image
+ *                   of the split query per request and group of 16 heads.
  *  stream           the plan's device metadata is uploaded on this stream
  *                   (stream-ordered before later runs on it).
  * Errors: MLA_ERR_INVALID_ARG / MLA_ERR_UNSUPPORTED before any allocation;
@@ -188,6 +188,88 @@ mla_status_t mla_decode_run_static_scratch(mla_plan_t plan, const void* q,
                                            float softmax_scale, void* out, float* lse,
                                            void* stream);
 
+/*
+ * mla_extend_plan -- plan() for causal extend attention over an FP8 cache:
+ * several new tokens per request (a prefill chunk on top of a cached prefix,
+ * or several speculative tokens), each attending to the request's cached
+ * history and to the new tokens before it.  This is the attention whose BF16
+ * requirement makes the FP8 configuration cast the whole history back to
+ * BF16 on every extend step ([P1] "Step 3: Source Validation", CastFromFP8);
+ * [P1] "From Attribution to Optimization Targets" asks for a prefill
+ * attention that reads the FP8 cache instead, which is what this plan runs.
+ * The pages do not spell the extend attention out; the reading implemented:
+ * request b has q_len_b = qo_indptr[b+1] - qo_indptr[b] new tokens, already
+ * stored in the cache (so seq_lens[b] counts them, q_len_b <= seq_lens[b]);
+ * new token i (0-based) sits at position seq_lens[b] - q_len_b + i and sees
+ * the tokens at positions 0 .. seq_lens[b] - q_len_b + i.  With every q_len
+ * equal to 1 this is exactly decode.
+ *  qo_indptr_host   int32 [batch+1], qo_indptr[0] = 0, non-decreasing: the
+ *                   new tokens of request b are query rows
+ *                   qo_indptr[b] .. qo_indptr[b+1]-1.
+ *  kv_indptr_host, seq_lens_host, num_heads, page_size
+ *                   as for mla_decode_plan.
+ *  kv_dtype         MLA_KV_FP8_E4M3 only (MLA_ERR_UNSUPPORTED otherwise).
+ *  workspace_bytes  out: scratch mla_extend_run needs (split partials and
+ *                   one split-query image per block of query rows).
+ * The query rows (new token x head, row = token * H + head) of each request
+ * are cut into blocks of 16 or 32 rows; each block runs like a decode
+ * request whose context ends at its last row's causal limit, rows of the
+ * block that see fewer tokens are masked.  Errors and plan lifetime as for
+ * mla_decode_plan (the plan must be rebuilt when qo_indptr changes too).  A
+ * plan made here is run with mla_extend_run only.
+ */
+mla_status_t mla_extend_plan(mla_plan_t* plan, const int32_t* qo_indptr_host,
+                             const int32_t* kv_indptr_host,
+                             const int32_t* seq_lens_host, int32_t batch,
+                             int32_t num_heads, int32_t page_size,
+                             mla_kv_dtype_t kv_dtype, size_t* workspace_bytes,
+                             void* stream);
+
+/*
+ * mla_extend_run -- run() for an extend plan.  For query row (n, h), n a new
+ * token of request b at position pos_n (see mla_extend_plan):
+ *     s_t = softmax_scale * sum_d q[n][h][d] * k_t[d],   t <= pos_n
+ *     out[n][h] = sum_{t <= pos_n} softmax(s)_t * v_t    (BF16)
+ *     lse[n][h] = ln sum_{t <= pos_n} exp(s_t)          (fp32)
+ * with k_t, v_t as in mla_decode_run.
+ *  q                BF16, element (n, h, d) at q + n*q_stride_tok +
+ *                   h*q_stride_h + d (elements; d < 576 contiguous), n <
+ *                   qo_indptr[batch].
+ *  out              BF16 [qo_indptr[batch]][H][512], contiguous.
+ *  lse              fp32 [qo_indptr[batch]][H], contiguous.
+ * Every other argument, the launches (query split, tcgen05 kernel, merge)
+ * and the errors are as for mla_decode_run; a decode plan is rejected
+ * (MLA_ERR_INVALID_ARG), as is an extend plan passed to mla_decode_run.
+ */
+mla_status_t mla_extend_run(mla_plan_t plan, const void* q, int64_t q_stride_tok,
+                            int64_t q_stride_h, const void* ckv_pool,
+                            int64_t ckv_row_stride_bytes, const void* kpe_pool,
+                            int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
+                            const int32_t* kv_indptr_dev,
+                            const int32_t* kv_indices_dev,
+                            const int32_t* seq_lens_dev, float k_scale,
+                            float softmax_scale, void* out, float* lse,
+                            void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * mla_extend_schedule -- host only: the schedule mla_extend_plan would build
+ * on a GPU with num_sms SMs.  segments_out (may be NULL): up to seg_capacity
+ * int32 quintuples (cta, block, token_begin, token_end, partial or -1);
+ * blocks_out (may be NULL): up to block_capacity int32 quadruples (request,
+ * first query row, rows, causal base: row r sees the tokens before
+ * base + r / H); counts_out (may be NULL): int32 [5] = segments, partials,
+ * CTAs, blocks, rows per block.  Validates exactly like mla_extend_plan.
+ */
+mla_status_t mla_extend_schedule(const int32_t* qo_indptr_host,
+                                 const int32_t* kv_indptr_host,
+                                 const int32_t* seq_lens_host, int32_t batch,
+                                 int32_t num_heads, int32_t page_size,
+                                 mla_kv_dtype_t kv_dtype, int32_t num_sms,
+                                 int32_t* segments_out, int32_t seg_capacity,
+                                 int32_t* blocks_out, int32_t block_capacity,
+                                 int32_t* counts_out, size_t* workspace_bytes);
+
 /* Releases a plan and its device / pinned buffers (after the caller has
  * synchronised any stream still using it).  NULL is accepted. */
 mla_status_t mla_decode_plan_destroy(mla_plan_t plan);
@@ -205,8 +287,9 @@ mla_status_t mla_decode_plan_info(mla_plan_t plan, int32_t* num_ctas,
  *     (cta, request, token_begin, token_end, partial_index or -1)
  * into segments_out (may be NULL), in launch order; tile_tokens receives the
  * kernel's tile (segments start on tile boundaries) and kernel the decode
- * kernel the plan would launch: 0 = mma.sync (BF16 pools, or more than 16
- * heads), 1 = tcgen05 on the E4M3 bytes (FP8 pools, up to 16 heads).  The
+ * kernel the plan would launch: 0 = mma.sync (BF16 pools), 1 = tcgen05 on
+ * the E4M3 bytes (FP8 pools; 16 heads per CTA, 32 when H is a multiple of
+ * 32, more heads as more CTAs).  The
  * mma.sync schedule gives each CTA an equal share of tiles; the tcgen05 one
  * balances tiles plus a fixed cost per segment.  Validates exactly like
  * mla_decode_plan.  Output pointers may be NULL.

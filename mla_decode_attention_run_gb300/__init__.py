@@ -18,7 +18,7 @@ __all__ = [
     "mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy", "mla_decode_plan_info",
     "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast", "mla_get_last_error",
     "exported_symbols", "D_CKV", "D_KPE", "D_QK", "mla_decode_run_static_scratch",
-    "STATIC_SCRATCH_BYTES",
+    "STATIC_SCRATCH_BYTES", "mla_extend_plan", "mla_extend_run", "mla_extend_schedule",
 ]
 
 D_CKV, D_KPE, D_QK = 512, 64, 576
@@ -62,6 +62,11 @@ def library():
     lib.mla_decode_plan_info.argtypes = [_P, _PI32, _PI32, _PI32, ctypes.POINTER(_sz)]
     lib.mla_decode_schedule.argtypes = [_P, _P, _i32, _i32, _i32, ctypes.c_int, _i32, _P, _i32,
                                         _PI32, _PI32, _PI32, _PI32, _PI32, ctypes.POINTER(_sz)]
+    lib.mla_extend_plan.argtypes = [ctypes.POINTER(_P), _P, _P, _P, _i32, _i32, _i32, ctypes.c_int,
+                                    ctypes.POINTER(_sz), _P]
+    lib.mla_extend_run.argtypes = lib.mla_decode_run.argtypes
+    lib.mla_extend_schedule.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_int, _i32, _P, _i32,
+                                        _P, _i32, _P, ctypes.POINTER(_sz)]
     lib.kv_store_fp8.argtypes = [_P, _P, _P, _i64, _f32, _P, _i64, _P, _i64, _i64, _P]
     lib.kv_gather_cast.argtypes = [_P, _i64, _P, _i64, _i64, _P, _i64, _i32, _f32, _P, _P, _P]
     lib.mla_get_last_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
@@ -69,7 +74,8 @@ def library():
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
                  "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
-                 "mla_get_last_error", "mla_decode_run_static_scratch"):
+                 "mla_get_last_error", "mla_decode_run_static_scratch", "mla_extend_plan",
+                 "mla_extend_run", "mla_extend_schedule"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -82,7 +88,8 @@ def exported_symbols() -> list[str]:
     names = []
     for n in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
               "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
-              "mla_get_last_error", "mla_status_string", "mla_decode_run_static_scratch"):
+              "mla_get_last_error", "mla_status_string", "mla_decode_run_static_scratch",
+              "mla_extend_plan", "mla_extend_run", "mla_extend_schedule"):
         getattr(lib, n)
         names.append(n)
     return names
@@ -211,6 +218,63 @@ def mla_decode_schedule(kv_indptr_host, seq_lens_host, batch: int, num_heads: in
            "mla_decode_schedule")
     return segs[:n.value], dict(num_ctas=c.value, num_partials=p.value, tile_tokens=t.value,
                                 kernel=k.value, workspace_bytes=w.value)
+
+
+def mla_extend_plan(qo_indptr_host, kv_indptr_host, seq_lens_host, batch: int, num_heads: int,
+                    page_size: int, kv_dtype: int = MLA_KV_FP8_E4M3, stream=None,
+                    plan: Plan | None = None) -> Plan:
+    """Plan causal extend attention: request b's new tokens are query rows
+    qo_indptr[b] .. qo_indptr[b+1]-1 and already count in seq_lens[b]."""
+    lib = library()
+    qo, indptr, lens = _host_i32(qo_indptr_host), _host_i32(kv_indptr_host), _host_i32(seq_lens_host)
+    plan = plan if plan is not None else Plan()
+    ws = _sz(0)
+    _check(lib.mla_extend_plan(ctypes.byref(plan.handle), qo.ctypes.data, indptr.ctypes.data,
+                               lens.ctypes.data, batch, num_heads, page_size, kv_dtype,
+                               ctypes.byref(ws), _stream(stream)), "mla_extend_plan")
+    plan.workspace_bytes = ws.value
+    plan._keep = (qo, indptr, lens)
+    return plan
+
+
+def mla_extend_run(plan: Plan, q, ckv_pool, kpe_pool, num_pool_slots: int, kv_indptr_dev,
+                   kv_indices_dev, seq_lens_dev, k_scale: float, softmax_scale: float, out, lse,
+                   workspace=None, stream=None):
+    """q: bf16 [n_q, H, 576] (contiguous last dim); out: bf16 [n_q, H, 512];
+    lse: fp32 [n_q, H]; the rest as mla_decode_run."""
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(library().mla_extend_run(plan.handle, q.data_ptr(), q.stride(0), q.stride(1),
+                                    ckv_pool.data_ptr(), _row_stride_bytes(ckv_pool),
+                                    kpe_pool.data_ptr(), _row_stride_bytes(kpe_pool),
+                                    num_pool_slots, kv_indptr_dev.data_ptr(),
+                                    _dptr(kv_indices_dev), seq_lens_dev.data_ptr(), k_scale,
+                                    softmax_scale, out.data_ptr(), lse.data_ptr(),
+                                    _dptr(workspace), ws_bytes, _stream(stream)),
+           "mla_extend_run")
+
+
+def mla_extend_schedule(qo_indptr_host, kv_indptr_host, seq_lens_host, batch: int,
+                        num_heads: int, page_size: int, kv_dtype: int = MLA_KV_FP8_E4M3,
+                        num_sms: int = 152):
+    """Host-only extend schedule: (segments int32 [n, 5] = cta, block, t0, t1,
+    partial; blocks int32 [m, 4] = request, first row, rows, causal base;
+    info dict)."""
+    lib = library()
+    qo, indptr, lens = _host_i32(qo_indptr_host), _host_i32(kv_indptr_host), _host_i32(seq_lens_host)
+    counts = np.zeros(5, np.int32)
+    w = _sz()
+    args = (qo.ctypes.data, indptr.ctypes.data, lens.ctypes.data, batch, num_heads, page_size,
+            kv_dtype, num_sms)
+    _check(lib.mla_extend_schedule(*args, None, 0, None, 0, counts.ctypes.data, ctypes.byref(w)),
+           "mla_extend_schedule")
+    segs = np.zeros((max(int(counts[0]), 1), 5), np.int32)
+    blocks = np.zeros((max(int(counts[3]), 1), 4), np.int32)
+    _check(lib.mla_extend_schedule(*args, segs.ctypes.data, int(counts[0]), blocks.ctypes.data,
+                                   int(counts[3]), counts.ctypes.data, ctypes.byref(w)),
+           "mla_extend_schedule")
+    return segs[:counts[0]], blocks[:counts[3]], dict(
+        num_segments=int(counts[0]), num_partials=int(counts[1]), num_ctas=int(counts[2]),
+        num_blocks=int(counts[3]), block_rows=int(counts[4]), workspace_bytes=w.value)
 
 
 def kv_store_fp8(ckv_new, kpe_new, slots, k_scale: float, ckv_pool, kpe_pool,

@@ -41,6 +41,34 @@ def decode_call_flops(seq_lens, heads: int) -> int:
     return int(np.asarray(seq_lens, np.int64).sum() * heads * 2 * (D_QK + D_CKV))
 
 
+def extend_visible_tokens(seq_lens, q_lens) -> int:
+    """Sum over new tokens of the tokens each sees: new token i of a request
+    with context L and q new tokens sees L - q + i + 1 of them."""
+    total = 0
+    for L, q in zip(np.asarray(seq_lens, np.int64), np.asarray(q_lens, np.int64)):
+        total += int(q * (L - q) + q * (q + 1) // 2)
+    return total
+
+
+def extend_call_bytes(seq_lens, q_lens, heads: int, page_size: int) -> int:
+    """Bytes one extend call must move: every KV row of every request with new
+    tokens once, its page-table entries, q, o and lse of every new token, and
+    qo_indptr, kv_indptr and seq_lens."""
+    lens = np.asarray(seq_lens, np.int64)
+    ql = np.asarray(q_lens, np.int64)
+    act = lens[ql > 0]
+    n_q = int(ql.sum())
+    B = lens.size
+    return int(act.sum() * D_QK + pages_of(act, page_size) * 4 + n_q * heads * (D_QK * 2 + D_CKV * 2 + 4)
+               + (3 * B + 2) * 4)
+
+
+def extend_call_flops(seq_lens, q_lens, heads: int) -> int:
+    """2 flops per multiply-add over the causally visible tokens of every new
+    token and head (576 for the score, 512 for the output)."""
+    return int(extend_visible_tokens(seq_lens, q_lens) * heads * 2 * (D_QK + D_CKV))
+
+
 def store_bytes(n_tokens: int) -> int:
     """Quantize-on-store: BF16 rows in (2 B/element), E4M3 rows out, slots."""
     return int(n_tokens * (D_QK * 2 + D_QK + 8))

@@ -382,29 +382,34 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
     }
 }
 
-// Combine split-KV partials: one warp per (request, head); lane i holds the
-// lse of partial i (per 32-partial chunk), the max and the weight sum are
-// warp-shuffle reductions, and each lane accumulates 16 output channels.
+// Combine split-KV partials: one warp per output row (request x head, or a
+// query block's row); lane i holds the lse of partial i (per 32-partial
+// chunk), the max and the weight sum are warp-shuffle reductions, and each
+// lane accumulates 16 output channels.  Entry e: output rows row0 .. row0 +
+// rows - 1 from partials first .. first + n - 1, row h of each at partial
+// row h (part_rows rows per partial).
 __global__ void __launch_bounds__(128)
-mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int heads,
+mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int part_rows,
                  const float* __restrict__ part_o, const float* __restrict__ part_lse,
                  uint16_t* __restrict__ out, float* __restrict__ lse) {
     griddep_wait();                                 // the decode kernel's partials are complete
     const int e = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * 4 + warp;
-    if (e >= n_merge || h >= heads) return;
-    const int b = merge[3 * e], first = merge[3 * e + 1], n = merge[3 * e + 2];
-    uint16_t* dst = out + (int64_t(b) * heads + h) * kDCkv + 16 * lane;
+    if (e >= n_merge) return;
+    const int row0 = merge[4 * e], first = merge[4 * e + 1], n = merge[4 * e + 2], rows = merge[4 * e + 3];
+    if (h >= rows) return;
+    const int64_t row = int64_t(row0) + h;
+    uint16_t* dst = out + row * kDCkv + 16 * lane;
     if (n == 0) {                                   // empty context: o = 0, lse = -inf
         reinterpret_cast<uint4*>(dst)[0] = make_uint4(0, 0, 0, 0);
         reinterpret_cast<uint4*>(dst)[1] = make_uint4(0, 0, 0, 0);
-        if (lane == 0) lse[int64_t(b) * heads + h] = -INFINITY;
+        if (lane == 0) lse[row] = -INFINITY;
         return;
     }
     float m = -INFINITY;
     for (int c = 0; c < n; c += 32)
-        if (c + lane < n) m = fmaxf(m, part_lse[int64_t(first + c + lane) * heads + h]);
+        if (c + lane < n) m = fmaxf(m, part_lse[int64_t(first + c + lane) * part_rows + h]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float acc[16];
@@ -412,13 +417,15 @@ mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int heads,
     for (int d = 0; d < 16; ++d) acc[d] = 0.f;
     float wsum = 0.f;
     for (int c = 0; c < n; c += 32) {
-        const float w = (c + lane < n) ? expf(part_lse[int64_t(first + c + lane) * heads + h] - m) : 0.f;
+        // a partial whose tokens the row cannot see (extend) has lse = -inf and
+        // o = 0: weight 0
+        const float w = (c + lane < n) ? expf(part_lse[int64_t(first + c + lane) * part_rows + h] - m) : 0.f;
         wsum += w;
         const int cnt = min(32, n - c);
         for (int i = 0; i < cnt; ++i) {
             const float wi = __shfl_sync(0xffffffffu, w, i);
             const float4* src =
-                reinterpret_cast<const float4*>(part_o + (int64_t(first + c + i) * heads + h) * kDCkv) + 4 * lane;
+                reinterpret_cast<const float4*>(part_o + (int64_t(first + c + i) * part_rows + h) * kDCkv) + 4 * lane;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float4 v = src[q];
@@ -437,7 +444,7 @@ mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int heads,
     for (int d = 0; d < 8; ++d) pk[d] = pack_bf16x2(acc[2 * d] * inv, acc[2 * d + 1] * inv);
     reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
     reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    if (lane == 0) lse[int64_t(b) * heads + h] = m + logf(wsum);
+    if (lane == 0) lse[row] = m + logf(wsum);
 }
 
 std::mutex g_attr_mu;
@@ -463,18 +470,22 @@ cudaError_t ensure_smem_attr() {
 }  // namespace
 }  // namespace mla
 
-extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q_stride_b,
-                                       int64_t q_stride_h, const void* ckv_pool,
-                                       int64_t ckv_row_stride_bytes, const void* kpe_pool,
-                                       int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
-                                       const int32_t* kv_indptr_dev, const int32_t* kv_indices_dev,
-                                       const int32_t* seq_lens_dev, float k_scale,
-                                       float softmax_scale, void* out, float* lse, void* workspace,
-                                       size_t workspace_bytes, void* stream) {
+namespace {
+
+// The run() half shared by decode and extend plans: checks, then the q split
+// + decode (+ merge) launches.  q_stride_b steps a request (decode) or a new
+// token (extend).
+mla_status_t run_plan(mla_plan_t plan, bool extend, const void* q, int64_t q_stride_b,
+                      int64_t q_stride_h, const void* ckv_pool, int64_t ckv_row_stride_bytes,
+                      const void* kpe_pool, int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
+                      const int32_t* kv_indptr_dev, const int32_t* kv_indices_dev,
+                      const int32_t* seq_lens_dev, float k_scale, float softmax_scale, void* out,
+                      float* lse, void* workspace, size_t workspace_bytes, void* stream) {
     using namespace mla;
     if (!plan || !q || !ckv_pool || !kpe_pool || !kv_indptr_dev || !seq_lens_dev || !out || !lse)
         return MLA_ERR_INVALID_ARG;
     const Schedule& s = plan->sched;
+    if (s.extend != extend) return MLA_ERR_INVALID_ARG;    // a decode plan for extend or back
     if (s.n_tokens > 0 && !kv_indices_dev) return MLA_ERR_INVALID_ARG;
     if (num_pool_slots < 0) return MLA_ERR_INVALID_ARG;
     if (!(k_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(softmax_scale))
@@ -521,6 +532,9 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
     p.qimg = static_cast<uint8_t*>(workspace) + s.qimg_offset;
     p.batch = s.batch;
     p.group_heads = s.group_heads;
+    p.part_rows = s.part_rows;
+    p.blocks = s.extend ? plan->dev_meta + plan->off_blocks : nullptr;
+    p.n_blocks = s.n_blocks();
 
     if (s.kernel == DecodeKernel::kTc && num_pool_slots >= INT32_MAX) return MLA_ERR_UNSUPPORTED;
     if (s.num_ctas > 0 && s.kernel == DecodeKernel::kTc) {
@@ -544,7 +558,7 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
         // processed while the decode's last CTAs finish, and its blocks wait
         // on the device for the decode's partials
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(s.n_merge(), (s.heads + 3) / 4);
+        cfg.gridDim = dim3(s.n_merge(), (s.part_rows + 3) / 4);
         cfg.blockDim = dim3(128);
         cfg.stream = cs;
         cudaLaunchAttribute attr[1];
@@ -553,10 +567,40 @@ extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         if (cudaLaunchKernelEx(&cfg, mla_merge_kernel, static_cast<const int32_t*>(plan->dev_meta + plan->off_merge),
-                               static_cast<int>(s.n_merge()), static_cast<int>(s.heads),
+                               static_cast<int>(s.n_merge()), static_cast<int>(s.part_rows),
                                static_cast<const float*>(p.part_o), static_cast<const float*>(p.part_lse), p.out,
                                p.lse) != cudaSuccess)
             return MLA_ERR_CUDA;
     }
     return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q_stride_b,
+                                       int64_t q_stride_h, const void* ckv_pool,
+                                       int64_t ckv_row_stride_bytes, const void* kpe_pool,
+                                       int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
+                                       const int32_t* kv_indptr_dev, const int32_t* kv_indices_dev,
+                                       const int32_t* seq_lens_dev, float k_scale,
+                                       float softmax_scale, void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    return run_plan(plan, false, q, q_stride_b, q_stride_h, ckv_pool, ckv_row_stride_bytes,
+                    kpe_pool, kpe_row_stride_bytes, num_pool_slots, kv_indptr_dev, kv_indices_dev,
+                    seq_lens_dev, k_scale, softmax_scale, out, lse, workspace, workspace_bytes,
+                    stream);
+}
+
+extern "C" mla_status_t mla_extend_run(mla_plan_t plan, const void* q, int64_t q_stride_tok,
+                                       int64_t q_stride_h, const void* ckv_pool,
+                                       int64_t ckv_row_stride_bytes, const void* kpe_pool,
+                                       int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
+                                       const int32_t* kv_indptr_dev, const int32_t* kv_indices_dev,
+                                       const int32_t* seq_lens_dev, float k_scale,
+                                       float softmax_scale, void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    return run_plan(plan, true, q, q_stride_tok, q_stride_h, ckv_pool, ckv_row_stride_bytes,
+                    kpe_pool, kpe_row_stride_bytes, num_pool_slots, kv_indptr_dev, kv_indices_dev,
+                    seq_lens_dev, k_scale, softmax_scale, out, lse, workspace, workspace_bytes,
+                    stream);
 }

@@ -29,6 +29,13 @@ struct DecodeParams {
     uint8_t* qimg;              // tcgen05 path: per-request q images (workspace)
     int32_t batch;
     int32_t group_heads;        // tcgen05 path: heads per CTA (16 or 32); grid.y = head_groups
+    int32_t part_rows;          // rows per partial slot (H; extend: group_heads)
+    // extend (causal, several new tokens per request): q / out / lse rows are
+    // token * H + head over all requests' new tokens, and the plan's segments
+    // name query blocks, 4 ints each: request, first row, rows, causal base
+    // (row r sees the tokens before base + r / H).  nullptr for decode.
+    const int32_t* blocks;
+    int32_t n_blocks;
 };
 
 // Launches the q split kernel and then, as its programmatic dependent, the

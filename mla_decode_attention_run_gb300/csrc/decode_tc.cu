@@ -110,7 +110,7 @@ struct Shape {
     static constexpr int kPBytes = (kN / 16) * kPUnit;    // [P1;P2]^T of one tile
     static constexpr int kHL = G / 2;                 // heads per softmax lane
     static constexpr uint32_t kColO = 2 * kN;         // TMEM: S[0], S[1], then O[b] + 4 kN b
-    static constexpr int kImage = kQBytes + G * 4;    // q image + score multipliers
+    static constexpr int kImage = kQBytes + G * 8;    // q image + score multipliers + causal limits
     static_assert(kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(kColO + kOBufs * 4 * kN <= kTmemCols, "TMEM columns");
 };
@@ -127,12 +127,12 @@ constexpr int kOffRing = kOffP + 2 * Shape<kMaxG>::kPBytes;   // kRing x 64 slot
 constexpr int kOffBar = kOffRing + kRing * kTT * 4;
 constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x G
 constexpr int kOffLsum = kOffRed + 2 * 4 * kMaxG * 4;   // softmax denominators: 4 warps x G
-constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // score multipliers (bulk-copy target)
-constexpr int kOffFlag = kOffCoef + 2 * 16 * 4;         // rescale votes: 2 x 4 warps
+constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // per q buffer: G multipliers, G limits
+constexpr int kOffFlag = kOffCoef + 2 * 16 * 8;         // rescale votes: 2 x 4 warps
 constexpr int kOffMisc = kOffFlag + 32;     // TMEM base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-static_assert(Shape<16>::kQBufs * 16 * 4 <= 2 * 16 * 4 && Shape<32>::kQBufs * 32 * 4 <= 2 * 16 * 4,
-              "multiplier space");
+static_assert(Shape<16>::kQBufs * 16 * 8 <= 2 * 16 * 8 && Shape<32>::kQBufs * 32 * 8 <= 2 * 16 * 8,
+              "multiplier and limit space");
 static_assert(Shape<16>::kImage == kTcQImageBytes && Shape<32>::kImage == 2 * kTcQImageBytes,
               "q image sizes the plan reserves");
 static_assert(kBlk % 1024 == 0 && kStage % 1024 == 0, "swizzle atoms need 1 KB alignment");
@@ -150,25 +150,32 @@ enum : int {
 static_assert(NUM_BARS * 8 <= 512, "barrier space");
 static_assert(SL_FULL == 23, "barrier count table below assumes four stages");
 
+// b: the request, or (extend) the query block; req: the request whose pages
+// and context the segment reads
 struct Seg {
-    int32_t b, t0, t1, part, ntiles;
+    int32_t b, req, t0, t1, part, ntiles;
 };
 
+// E: extend plan (segments name query blocks); the decode kernels are
+// compiled without the indirection
+template <bool E>
 __device__ __forceinline__ Seg load_seg(const DecodeParams& p, int si) {
     Seg s;
     s.b = p.segs[4 * si];
     s.t0 = p.segs[4 * si + 1];
     s.t1 = p.segs[4 * si + 2];
     s.part = p.segs[4 * si + 3];
+    s.req = E ? p.blocks[4 * s.b] : s.b;
     // a segment longer than the device-side context means the page table
     // changed after planning: it is skipped (and flagged by the MMA thread)
-    s.ntiles = s.t1 <= p.seq_lens[s.b] ? (s.t1 - s.t0 + kTT - 1) / kTT : 0;
+    s.ntiles = s.t1 <= p.seq_lens[s.req] ? (s.t1 - s.t0 + kTT - 1) / kTT : 0;
     return s;
 }
 
+template <bool E>
 __device__ __forceinline__ int count_tiles(const DecodeParams& p, int lo, int hi) {
     int n = 0;
-    for (int si = lo; si < hi; ++si) n += load_seg(p, si).ntiles;
+    for (int si = lo; si < hi; ++si) n += load_seg<E>(p, si).ntiles;
     return n;
 }
 
@@ -191,6 +198,7 @@ constexpr int32_t kNoRow = INT32_MIN;
 
 // Cursor over the tiles of a CTA's segments, with the raw page entries of
 // rows 2 lane, 2 lane + 1 of one tile.
+template <bool E>
 struct TileCursor {
     int si, seg_hi, it;
     Seg sg;
@@ -202,8 +210,8 @@ struct TileCursor {
         si = lo;
         seg_hi = hi;
         it = 0;
-        while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
-        if (si < seg_hi) pages = p.indices + p.indptr[sg.b];
+        while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
+        if (si < seg_hi) pages = p.indices + p.indptr[sg.req];
     }
     __device__ bool valid() const { return si < seg_hi; }
     // issue the (independent) index loads of the current tile; nothing waits
@@ -230,8 +238,8 @@ struct TileCursor {
         if (++it == sg.ntiles) {
             it = 0;
             ++si;
-            while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
-            if (si < seg_hi) pages = p.indices + p.indptr[sg.b];
+            while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
+            if (si < seg_hi) pages = p.indices + p.indptr[sg.req];
         }
     }
 };
@@ -263,12 +271,13 @@ __device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage
     }
 }
 
+template <bool E>
 __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                           int seg_lo, int seg_hi, int lane) {
     int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
     // one prefetch sweep per row when k_pe follows c_kv in the same row
     const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
-    TileCursor cur;
+    TileCursor<E> cur;
     cur.init(p, seg_lo, seg_hi);
     if (cur.valid()) cur.prefetch(p, lane);
     // publishes every tile as soon as its ring entry is free (the ring bounds
@@ -298,10 +307,11 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     }
 }
 
+template <bool E>
 __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                           int seg_lo, int seg_hi, int w, int lane) {
     const int32_t* ring = reinterpret_cast<const int32_t*>(base + kOffRing);
-    const int total = count_tiles(p, seg_lo, seg_hi);
+    const int total = count_tiles<E>(p, seg_lo, seg_hi);
     for (int i = 0; i < total; ++i) {
         const int slot = i % kStages;
         const uint32_t u = static_cast<uint32_t>(i / kStages);
@@ -384,6 +394,7 @@ __device__ __forceinline__ void issue_pv(const MmaCtx& c, int j, int ob, bool fi
 }
 
 // Position in the CTA's tile sequence: segment ordinal k and tile it of it.
+template <bool E>
 struct SegWalk {
     int si, seg_hi, it, k;
     Seg sg;
@@ -392,14 +403,14 @@ struct SegWalk {
         seg_hi = hi;
         it = 0;
         k = 0;
-        while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
+        while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
     }
     __device__ void advance(const DecodeParams& p) {
         if (++it == sg.ntiles) {
             it = 0;
             ++k;
             ++si;
-            while (si < seg_hi && (sg = load_seg(p, si)).ntiles == 0) ++si;
+            while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
         }
     }
 };
@@ -409,16 +420,16 @@ struct SegWalk {
 // PV of tile i queued behind QK^T of tile i + 1 (and freed its stage late);
 // with two, each goes out as soon as its inputs are ready.  QK^T needs its
 // stage full, so it runs at most a stage ahead of PV by construction.
-template <int G>
+template <int G, bool E>
 __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
     using S = Shape<G>;
     int total = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
-        const Seg sg = load_seg(p, si);
+        const Seg sg = load_seg<E>(p, si);
         if (sg.ntiles == 0 && sg.t1 > sg.t0) raise_flag(p.flags, MLA_FLAG_PLAN_MISMATCH);
         total += sg.ntiles;
     }
-    SegWalk wq;
+    SegWalk<E> wq;
     wq.init(p, seg_lo, seg_hi);
     for (int qk = 0; qk < total; ++qk) {
         const int slot = qk & 1;
@@ -442,11 +453,11 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
     mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
 }
 
-template <int G>
+template <int G, bool E>
 __device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
     using S = Shape<G>;
-    const int total = count_tiles(p, seg_lo, seg_hi);
-    SegWalk wp;
+    const int total = count_tiles<E>(p, seg_lo, seg_hi);
+    SegWalk<E> wp;
     wp.init(p, seg_lo, seg_hi);
     for (int pv = 0; pv < total; ++pv) {
         const int ob = wp.k % S::kOBufs;
@@ -510,20 +521,35 @@ __device__ __forceinline__ float amax_bf16x8(const uint4& v, float a) {
 
 constexpr int kSplitThreads = 64;
 
-// One warp per (request, head row): lane c splits 16-channel chunk c of c_kv,
-// lanes 0-3 also chunk c of k_pe.  Heads are taken in groups of G, one image
-// per (request, group); heads >= H get zero rows and multiplier 0.
+// One warp per image row: lane c splits 16-channel chunk c of c_kv, lanes 0-3
+// also chunk c of k_pe.  Decode: one image per (request, group of G heads);
+// heads >= H get zero rows and multiplier 0.  Extend: one image per query
+// block, row r = block row r (token row / H, head row % H); rows past the
+// block's end are zero.  Each valid row also gets its causal limit.
 template <int G>
 __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const DecodeParams p) {
     using S = Shape<G>;
     griddep_launch_dependents();                // the decode kernel may start loading KV now
     const int wg = (blockIdx.x * kSplitThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int rows = p.head_groups * G;
-    const int b = wg / rows, head = wg % rows, r = head % G;
-    if (b >= p.batch) return;
-    const bool valid = head < p.heads;
+    const int image = wg / G, r = wg % G;
+    if (image >= (p.blocks ? p.n_blocks : p.batch * p.head_groups)) return;
+    int64_t tok;
+    int head, lim = 0;
+    bool valid;
+    if (p.blocks) {
+        const int32_t* blk = p.blocks + 4 * image;
+        valid = r < blk[2];
+        const int row = blk[1] + (valid ? r : 0);
+        tok = row / p.heads;
+        head = row % p.heads;
+        lim = blk[3] + static_cast<int>(tok);
+    } else {
+        tok = image / p.head_groups;
+        head = (image % p.head_groups) * G + r;
+        valid = head < p.heads;
+    }
     const uint4* src =
-        reinterpret_cast<const uint4*>(p.q + int64_t(b) * p.q_sb + int64_t(valid ? head : 0) * p.q_sh);
+        reinterpret_cast<const uint4*>(p.q + tok * p.q_sb + int64_t(valid ? head : 0) * p.q_sh);
     const uint4 z = make_uint4(0, 0, 0, 0);
     const uint4 va = valid ? src[2 * lane] : z, vb = valid ? src[2 * lane + 1] : z;
     const bool rope = lane < 4;
@@ -536,7 +562,7 @@ __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const Decode
     int sigma = amax > 0.f ? 8 - e2 : 0;            // max |q| * 2^sigma in [128, 256)
     sigma = sigma > 100 ? 100 : (sigma < -100 ? -100 : sigma);
     const float scale = ldexpf(1.f, sigma);
-    uint8_t* img = p.qimg + (int64_t(b) * p.head_groups + head / G) * S::kImage;
+    uint8_t* img = p.qimg + int64_t(image) * S::kImage;
     const int row1 = r, row2 = G + r;
     uint4 t1, t2;
     split_chunk(va, vb, scale, t1, t2);
@@ -550,14 +576,16 @@ __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const Decode
         *reinterpret_cast<uint4*>(img + 4 * S::kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4)) = t1;
         *reinterpret_cast<uint4*>(img + 4 * S::kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4)) = t2;
     }
-    if (lane == 0)
+    if (lane == 0) {
         reinterpret_cast<float*>(img + S::kQBytes)[r] =
             valid ? ldexpf(p.softmax_scale * p.k_scale * kLog2e, -sigma) : 0.f;
+        reinterpret_cast<int32_t*>(img + S::kQBytes)[G + r] = valid ? lim : 0;
+    }
 }
 
 // Warp 5: fetches each segment's q image into its q buffer (and the
 // multipliers) once the split kernel has finished.
-template <int G>
+template <int G, bool E>
 __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                         int seg_lo, int seg_hi, int lane) {
     using S = Shape<G>;
@@ -565,15 +593,16 @@ __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, vo
     griddep_wait();                                 // the q images are complete
     int k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
-        const Seg sg = load_seg(p, si);
+        const Seg sg = load_seg<E>(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k % S::kQBufs;
         const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
         if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
-        const uint8_t* img = p.qimg + (int64_t(sg.b) * p.head_groups + blockIdx.y) * S::kImage;
+        const int64_t image = E ? sg.b : int64_t(sg.b) * p.head_groups + blockIdx.y;
+        const uint8_t* img = p.qimg + image * S::kImage;
         mbar_arrive_expect_tx(&bars[Q_FULL + qs], S::kImage);
         bulk_copy_g2s(smem_u32(base + kOffQ + qs * S::kQBytes), img, S::kQBytes, &bars[Q_FULL + qs]);
-        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * G * 4), img + S::kQBytes, G * 4, &bars[Q_FULL + qs]);
+        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * G * 8), img + S::kQBytes, G * 8, &bars[Q_FULL + qs]);
         ++k;
     }
     // copies in flight (after an abort) land before the CTA exits
@@ -659,7 +688,7 @@ __device__ __forceinline__ int half_reduce_index(int lane) { return V == 16 ? (l
 template <int V>
 __device__ __forceinline__ bool half_reduce_writer(int lane) { return V == 16 || (lane & 1) == 0; }
 
-template <int G>
+template <int G, bool E>
 __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, int seg_hi, int head0) {
     using S = Shape<G>;
     constexpr int kHL = S::kHL;
@@ -674,15 +703,19 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
     // abort flag is set every wait returns at once and the results are void.
     int i = 0, k = 0;
     for (int si = seg_lo; si < seg_hi; ++si) {
-        const Seg sg = load_seg(p, si);
+        const Seg sg = load_seg<E>(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k % S::kQBufs;
         const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
         const uint32_t ocol = S::kColO + 4 * S::kN * (k % S::kOBufs);
         mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags);
-        // the segment's score multipliers stay in shared memory (its q buffer
-        // is released at the end of the segment)
-        const float* coef = coefs + qs * G;
+        // the segment's score multipliers and causal limits stay in shared
+        // memory (its q buffer is released at the end of the segment)
+        const float* coef = coefs + qs * 2 * G;
+        const int32_t* lim = reinterpret_cast<const int32_t*>(coef + G);
+        // extend: tiles reaching the first row's limit need the causal mask
+        // (rows are in token order, so the first row's limit is the lowest)
+        const int mask_from = E ? lim[0] : INT32_MAX;
 
         float m[kHL], l[kHL];                       // heads hb .. hb + kHL - 1
 #pragma unroll
@@ -722,14 +755,24 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
 
             // the second half of the heads moves to lanes 16-31
             float s[kHL];
-            bool need = false;
 #pragma unroll
             for (int j = 0; j < kHL; ++j) {
                 const float hi = __shfl_sync(0xffffffffu, sum[kHL + j], w.lane & 15);
                 const float raw = w.hb ? hi : sum[j];
                 s[j] = valid ? raw * coef[w.hb + j] : -INFINITY;
-                need |= s[j] > m[j] + kTau;         // always true on a segment's first tile
             }
+            if constexpr (E) {
+                const int tile_t0 = sg.t0 + it * kTT;
+                if (tile_t0 + kTT > mask_from) {    // token tile_t0 + srow is hidden from rows
+                    const int t = tile_t0 + w.srow; // whose limit it reaches
+#pragma unroll
+                    for (int j = 0; j < kHL; ++j)
+                        if (t >= lim[w.hb + j]) s[j] = -INFINITY;
+                }
+            }
+            bool need = false;
+#pragma unroll
+            for (int j = 0; j < kHL; ++j) need |= s[j] > m[j] + kTau;   // true on a segment's first tile
             // the running maximum moves only if some score got more than
             // 2^kTau above it (one vote per warp, then one barrier)
             need = __any_sync(0xffffffffu, need);
@@ -828,7 +871,19 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         const int jl = i - 1;                       // the segment's last tile
         mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
-        const int H = p.heads;
+        // output rows row0 .. row0 + nrows - 1; a partial slot holds
+        // p.part_rows rows, this CTA's from prow0
+        int64_t row0;
+        int nrows, prow0;
+        if constexpr (E) {
+            row0 = p.blocks[4 * sg.b + 1];
+            nrows = p.blocks[4 * sg.b + 2];
+            prow0 = 0;
+        } else {
+            row0 = int64_t(sg.b) * p.heads + head0;
+            nrows = p.heads - head0 < G ? p.heads - head0 : G;
+            prow0 = head0;
+        }
         // o and l are both in units of p * kPScale; lse = m + log2(sum p)
         const float lse_off = -kTau;                 // kPScale = 2^kTau
 #pragma unroll 1
@@ -850,17 +905,17 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             }
             const int ch = mb * 128 + w.row;
             if (sg.part < 0) {
-                uint16_t* out = p.out + (int64_t(sg.b) * H + head0) * kDCkv + ch;
+                uint16_t* out = p.out + int64_t(row0) * kDCkv + ch;
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    if (head0 + h >= H) break;
+                    if (h >= nrows) break;
                     out[h * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h] * inv[h]));
                 }
             } else {
-                float* po = p.part_o + (int64_t(sg.part) * H + head0) * kDCkv + ch;
+                float* po = p.part_o + (int64_t(sg.part) * p.part_rows + prow0) * kDCkv + ch;
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
-                    if (head0 + h >= H) break;
+                    if (h >= nrows) break;
                     po[h * kDCkv] = o[h] * inv[h];
                 }
             }
@@ -869,16 +924,16 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         mbar_arrive(&w.bars[O_FREE + (k % S::kOBufs)]);   // a later segment may overwrite O
         mbar_arrive(&w.bars[Q_FREE + qs]);
         if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb + kHL - 1
-            float* dst = sg.part < 0 ? p.lse + int64_t(sg.b) * H : p.part_lse + int64_t(sg.part) * H;
+            float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
 #pragma unroll
             for (int j = 0; j < kHL; ++j)
-                if (head0 + w.hb + j < H) dst[head0 + w.hb + j] = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
+                if (w.hb + j < nrows) dst[w.hb + j] = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
         }
         ++k;
     }
 }
 
-template <int G>
+template <int G, bool E>
 __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const DecodeParams p) {
     using S = Shape<G>;
     extern __shared__ uint8_t smem_raw[];
@@ -911,9 +966,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == kWarpSched) {
-        scheduler(p, base, bars, abort, seg_lo, seg_hi, lane);
+        scheduler<E>(p, base, bars, abort, seg_lo, seg_hi, lane);
     } else if (warp < kFillWarps) {
-        fill_warp(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
+        fill_warp<E>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
     } else if (warp == kWarpMma || warp == kWarpPv) {
         if (lane == 0) {
             MmaCtx c;
@@ -924,12 +979,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
             c.bars = bars;
             c.abort = abort;
             c.flags = p.flags;
-            if (warp == kWarpMma) qk_issuer<G>(p, c, seg_lo, seg_hi);
-            else pv_issuer<G>(p, c, seg_lo, seg_hi);
+            if (warp == kWarpMma) qk_issuer<G, E>(p, c, seg_lo, seg_hi);
+            else pv_issuer<G, E>(p, c, seg_lo, seg_hi);
         }
         __syncwarp();
     } else if (warp == kWarpQ) {
-        q_fetch<G>(p, base, bars, abort, seg_lo, seg_hi, lane);
+        q_fetch<G, E>(p, base, bars, abort, seg_lo, seg_hi, lane);
     } else {                                      // warps kWarpWg .. kWarpWg + 3
         WgCtx w;
         w.base = base;
@@ -943,7 +998,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
         w.hb = (lane >> 4) * S::kHL;
         w.wq = warp - kWarpWg;
         w.lane = lane;
-        softmax_wg<G>(p, w, seg_lo, seg_hi, head0);
+        softmax_wg<G, E>(p, w, seg_lo, seg_hi, head0);
     }
     fence_before_sync();
     __syncthreads();
@@ -955,22 +1010,23 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const Decode
 }
 
 std::mutex g_mu;
-std::vector<char> g_attr;     // per device: bit 0 / 1: max dynamic smem set for G = 16 / 32
+std::vector<char> g_attr;     // per device: bit (G / 16 - 1) + 2 E: max dynamic smem set
 
-template <int G>
+template <int G, bool E>
 cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int dev) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if ((int)g_attr.size() <= dev) g_attr.resize(dev + 1, 0);
-        const char bit = G == 16 ? 1 : 2;
+        const char bit = static_cast<char>(1 << ((G / 16 - 1) + 2 * E));
         if (!(g_attr[dev] & bit)) {
-            const cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<G>,
+            const cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<G, E>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
             g_attr[dev] |= bit;
         }
     }
-    const int split_blocks = (p.batch * p.head_groups * G * 32 + kSplitThreads - 1) / kSplitThreads;
+    const int64_t images = E ? p.n_blocks : int64_t(p.batch) * p.head_groups;
+    const int split_blocks = static_cast<int>((images * G * 32 + kSplitThreads - 1) / kSplitThreads);
     mla_q_split_kernel<G><<<split_blocks, kSplitThreads, 0, stream>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -985,7 +1041,7 @@ cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int d
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G>, p);
+    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G, E>, p);
 }
 
 }  // namespace
@@ -996,8 +1052,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t strea
     if (e != cudaSuccess) return e;
     // slots are held as int32 in the kernel's shared slot lists
     if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
-    if (p.group_heads == 32) return launch_g<32>(p, grid, stream, dev);
-    if (p.group_heads == 16) return launch_g<16>(p, grid, stream, dev);
+    const bool ext = p.blocks != nullptr;
+    if (p.group_heads == 32) return ext ? launch_g<32, true>(p, grid, stream, dev) : launch_g<32, false>(p, grid, stream, dev);
+    if (p.group_heads == 16) return ext ? launch_g<16, true>(p, grid, stream, dev) : launch_g<16, false>(p, grid, stream, dev);
     return cudaErrorInvalidValue;
 }
 

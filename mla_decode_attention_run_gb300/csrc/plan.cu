@@ -98,6 +98,21 @@ void build_cost_balanced(const int32_t* seq, int32_t B, int64_t tile, int64_t ma
     s.cta_ptr[s.num_ctas] = static_cast<int32_t>(s.segs.size() / 4);
 }
 
+// Workspace: partials (o, then lse) for part_rows rows each, then, on the
+// tcgen05 path, one q image per (request, head group) or query block.
+void size_workspace(Schedule& s, int64_t images) {
+    const size_t o_bytes = static_cast<size_t>(s.n_partials) * s.part_rows * kDCkv * sizeof(float);
+    s.partial_lse_offset = align256(o_bytes);
+    s.workspace_bytes =
+        s.n_partials ? align256(s.partial_lse_offset + static_cast<size_t>(s.n_partials) * s.part_rows * 4)
+                     : 0;
+    if (s.kernel == DecodeKernel::kTc && s.num_ctas > 0) {
+        s.qimg_offset = s.workspace_bytes;
+        s.workspace_bytes =
+            align256(s.qimg_offset + static_cast<size_t>(images) * (s.group_heads / 16) * kTcQImageBytes);
+    }
+}
+
 }  // namespace
 
 mla_status_t validate_plan_inputs(const int32_t* indptr, const int32_t* seq, int32_t B,
@@ -186,20 +201,102 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
         }
     }
     for (int32_t r = 0; r < B; ++r) {
-        if (segs_per_req[r] > 1) s.merge.insert(s.merge.end(), {r, first_partial[r], segs_per_req[r]});
-        else if (seq[r] == 0) s.merge.insert(s.merge.end(), {r, 0, 0});
+        if (segs_per_req[r] > 1) s.merge.insert(s.merge.end(), {r * H, first_partial[r], segs_per_req[r], H});
+        else if (seq[r] == 0) s.merge.insert(s.merge.end(), {r * H, 0, 0, H});
     }
+    s.part_rows = H;
+    size_workspace(s, static_cast<int64_t>(B) * s.head_groups);
+    return MLA_OK;
+}
 
-    const size_t o_bytes = static_cast<size_t>(s.n_partials) * H * kDCkv * sizeof(float);
-    s.partial_lse_offset = align256(o_bytes);
-    s.workspace_bytes =
-        s.n_partials ? align256(s.partial_lse_offset + static_cast<size_t>(s.n_partials) * H * 4) : 0;
-    if (kernel == DecodeKernel::kTc && s.num_ctas > 0) {
-        s.qimg_offset = s.workspace_bytes;
-        s.workspace_bytes =
-            align256(s.qimg_offset + static_cast<size_t>(B) * s.head_groups * (s.group_heads / 16) *
-                                         kTcQImageBytes);
+mla_status_t validate_extend_inputs(const int32_t* qo, const int32_t* indptr, const int32_t* seq,
+                                    int32_t B, int32_t H, int32_t ps, mla_kv_dtype_t dtype) {
+    if (!qo) return MLA_ERR_INVALID_ARG;
+    const mla_status_t st = validate_plan_inputs(indptr, seq, B, H, ps, dtype);
+    if (st != MLA_OK) return st;
+    // the extend kernel reads E4M3 pools only (the BF16-pool kernel is decode only)
+    if (dtype != MLA_KV_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+    if (qo[0] != 0) return MLA_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t n = static_cast<int64_t>(qo[b + 1]) - qo[b];
+        if (n < 0 || n > seq[b]) return MLA_ERR_INVALID_ARG;
     }
+    // rows (token x head) are int32 on the device
+    if (static_cast<int64_t>(qo[B]) * H >= INT32_MAX) return MLA_ERR_UNSUPPORTED;
+    return MLA_OK;
+}
+
+mla_status_t build_extend_schedule(const int32_t* qo, const int32_t* indptr, const int32_t* seq,
+                                   int32_t B, int32_t H, int32_t ps, mla_kv_dtype_t dtype,
+                                   int32_t num_sms, Schedule& s) {
+    const mla_status_t st = validate_extend_inputs(qo, indptr, seq, B, H, ps, dtype);
+    if (st != MLA_OK) return st;
+    if (num_sms < 1) return MLA_ERR_INVALID_ARG;
+    s = Schedule();
+    s.batch = B;
+    s.heads = H;
+    s.page_size = ps;
+    s.kv_dtype = dtype;
+    s.kernel = DecodeKernel::kTc;
+    s.tile_tokens = kTcTileTokens;
+    s.extend = true;
+    s.n_q = qo[B];
+    s.head_groups = 1;
+
+    // Query rows of request b: row = token * H + head over its new tokens.
+    // Blocks of 32 rows when that needs clearly fewer blocks than 16 (an
+    // N = 64 MMA costs what N = 32 does; the softmax pays per row)
+    int64_t blocks16 = 0, blocks32 = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t rows = (static_cast<int64_t>(qo[b + 1]) - qo[b]) * H;
+        blocks16 += (rows + 15) / 16;
+        blocks32 += (rows + 31) / 32;
+    }
+    s.group_heads = 4 * blocks32 <= 3 * blocks16 ? 32 : kHeadsPerCta;
+    const int64_t G = s.group_heads;
+
+    // each block is scheduled like a request whose context ends at the
+    // causal limit of its last row
+    std::vector<int32_t> len;
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t r_lo = static_cast<int64_t>(qo[b]) * H, r_hi = static_cast<int64_t>(qo[b + 1]) * H;
+        // row r (token r / H) sees the tokens before base + r / H: the last
+        // new token sees the whole context
+        const int64_t base = static_cast<int64_t>(seq[b]) + 1 - qo[b + 1];
+        for (int64_t r0 = r_lo; r0 < r_hi; r0 += G) {
+            const int64_t rows = r_hi - r0 < G ? r_hi - r0 : G;
+            s.blocks.insert(s.blocks.end(), {b, static_cast<int32_t>(r0), static_cast<int32_t>(rows),
+                                             static_cast<int32_t>(base)});
+            len.push_back(static_cast<int32_t>(base + (r0 + rows - 1) / H));
+        }
+    }
+    const int32_t nb = s.n_blocks();
+    int64_t n_tiles = 0;
+    for (int32_t v = 0; v < nb; ++v) {
+        s.n_tokens += len[v];
+        n_tiles += (len[v] + kTcTileTokens - 1) / kTcTileTokens;
+    }
+    int64_t ctas = num_sms;
+    const int64_t by_work = (n_tiles + min_tiles_per_cta(DecodeKernel::kTc) - 1) /
+                            min_tiles_per_cta(DecodeKernel::kTc);
+    if (ctas > by_work) ctas = by_work;
+    std::vector<int32_t> segs_per_block(nb, 0);
+    build_cost_balanced(len.data(), nb, kTcTileTokens, ctas, s, segs_per_block);
+
+    std::vector<int32_t> first_partial(nb, -1);
+    for (int32_t i = 0; i < s.n_segs(); ++i) {
+        const int32_t v = s.segs[4 * i];
+        if (segs_per_block[v] > 1) {
+            if (first_partial[v] < 0) first_partial[v] = s.n_partials;
+            s.segs[4 * i + 3] = s.n_partials++;
+        }
+    }
+    for (int32_t v = 0; v < nb; ++v)
+        if (segs_per_block[v] > 1)
+            s.merge.insert(s.merge.end(), {s.blocks[4 * v + 1], first_partial[v], segs_per_block[v],
+                                           s.blocks[4 * v + 2]});
+    s.part_rows = static_cast<int32_t>(G);
+    size_workspace(s, nb);
     return MLA_OK;
 }
 
@@ -238,6 +335,44 @@ extern "C" mla_status_t mla_decode_schedule(const int32_t* kv_indptr_host,
     return MLA_OK;
 }
 
+extern "C" mla_status_t mla_extend_schedule(const int32_t* qo_indptr_host,
+                                            const int32_t* kv_indptr_host,
+                                            const int32_t* seq_lens_host, int32_t batch,
+                                            int32_t num_heads, int32_t page_size,
+                                            mla_kv_dtype_t kv_dtype, int32_t num_sms,
+                                            int32_t* segments_out, int32_t seg_capacity,
+                                            int32_t* blocks_out, int32_t block_capacity,
+                                            int32_t* counts_out, size_t* workspace_bytes) {
+    Schedule s;
+    const mla_status_t st = mla::build_extend_schedule(qo_indptr_host, kv_indptr_host,
+                                                       seq_lens_host, batch, num_heads, page_size,
+                                                       kv_dtype, num_sms, s);
+    if (st != MLA_OK) return st;
+    if (segments_out) {
+        int32_t k = 0;
+        for (int32_t c = 0; c < s.num_ctas; ++c) {
+            for (int32_t i = s.cta_ptr[c]; i < s.cta_ptr[c + 1] && k < seg_capacity; ++i, ++k) {
+                int32_t* d = segments_out + 5 * k;
+                d[0] = c;
+                std::memcpy(d + 1, &s.segs[4 * i], 4 * sizeof(int32_t));
+            }
+        }
+    }
+    if (blocks_out) {
+        const int32_t n = s.n_blocks() < block_capacity ? s.n_blocks() : block_capacity;
+        if (n > 0) std::memcpy(blocks_out, s.blocks.data(), 4 * sizeof(int32_t) * n);
+    }
+    if (counts_out) {
+        counts_out[0] = s.n_segs();
+        counts_out[1] = s.n_partials;
+        counts_out[2] = s.num_ctas;
+        counts_out[3] = s.n_blocks();
+        counts_out[4] = s.group_heads;
+    }
+    if (workspace_bytes) *workspace_bytes = s.workspace_bytes;
+    return MLA_OK;
+}
+
 namespace {
 
 void release_buffers(mla_plan* p) {
@@ -252,24 +387,13 @@ void release_buffers(mla_plan* p) {
 
 }  // namespace
 
-extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indptr_host,
-                                        const int32_t* seq_lens_host, int32_t batch,
-                                        int32_t num_heads, int32_t page_size,
-                                        mla_kv_dtype_t kv_dtype, size_t* workspace_bytes,
-                                        void* stream) {
-    if (!plan || !workspace_bytes) return MLA_ERR_INVALID_ARG;
-    mla_status_t st = mla::validate_plan_inputs(kv_indptr_host, seq_lens_host, batch, num_heads,
-                                                page_size, kv_dtype);
-    if (st != MLA_OK) return st;
+namespace {
+
+// Makes (or refills) the plan handle and uploads the schedule's device tables
+// (CTA ranges, segments, merge entries, query blocks) with one async copy.
+mla_status_t install(mla_plan_t* plan, Schedule&& s, size_t* workspace_bytes, void* stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
-    const int sms = mla::device_sm_count();
-    if (sms <= 0) return MLA_ERR_CUDA;
-    Schedule s;
-    st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads, page_size,
-                             kv_dtype, sms, s);
-    if (st != MLA_OK) return st;
-
     mla_plan* p = *plan;
     const bool fresh = (p == nullptr);
     if (fresh) {
@@ -279,7 +403,8 @@ extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indp
         return MLA_ERR_INVALID_ARG;       // a plan belongs to one device
     }
     p->device = dev;
-    const size_t need = static_cast<size_t>(s.num_ctas + 1) + s.segs.size() + s.merge.size();
+    const size_t need =
+        static_cast<size_t>(s.num_ctas + 1) + s.segs.size() + s.merge.size() + s.blocks.size();
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
     if (!p->upload_done &&
@@ -321,11 +446,14 @@ extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indp
     p->off_cta = 0;
     p->off_segs = s.num_ctas + 1;
     p->off_merge = p->off_segs + s.segs.size();
+    p->off_blocks = p->off_merge + s.merge.size();
     std::memcpy(p->pinned + p->off_cta, s.cta_ptr.data(), (s.num_ctas + 1) * sizeof(int32_t));
     if (!s.segs.empty())
         std::memcpy(p->pinned + p->off_segs, s.segs.data(), s.segs.size() * sizeof(int32_t));
     if (!s.merge.empty())
         std::memcpy(p->pinned + p->off_merge, s.merge.data(), s.merge.size() * sizeof(int32_t));
+    if (!s.blocks.empty())
+        std::memcpy(p->pinned + p->off_blocks, s.blocks.data(), s.blocks.size() * sizeof(int32_t));
     if (cudaMemcpyAsync(p->dev_meta, p->pinned, need * sizeof(int32_t), cudaMemcpyHostToDevice,
                         cs) != cudaSuccess ||
         cudaEventRecord(p->upload_done, cs) != cudaSuccess) {
@@ -336,6 +464,45 @@ extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indp
     *workspace_bytes = p->sched.workspace_bytes;
     *plan = p;
     return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indptr_host,
+                                        const int32_t* seq_lens_host, int32_t batch,
+                                        int32_t num_heads, int32_t page_size,
+                                        mla_kv_dtype_t kv_dtype, size_t* workspace_bytes,
+                                        void* stream) {
+    if (!plan || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+    mla_status_t st = mla::validate_plan_inputs(kv_indptr_host, seq_lens_host, batch, num_heads,
+                                                page_size, kv_dtype);
+    if (st != MLA_OK) return st;
+    const int sms = mla::device_sm_count();
+    if (sms <= 0) return MLA_ERR_CUDA;
+    Schedule s;
+    st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads, page_size,
+                             kv_dtype, sms, s);
+    if (st != MLA_OK) return st;
+    return install(plan, std::move(s), workspace_bytes, stream);
+}
+
+extern "C" mla_status_t mla_extend_plan(mla_plan_t* plan, const int32_t* qo_indptr_host,
+                                        const int32_t* kv_indptr_host,
+                                        const int32_t* seq_lens_host, int32_t batch,
+                                        int32_t num_heads, int32_t page_size,
+                                        mla_kv_dtype_t kv_dtype, size_t* workspace_bytes,
+                                        void* stream) {
+    if (!plan || !workspace_bytes) return MLA_ERR_INVALID_ARG;
+    mla_status_t st = mla::validate_extend_inputs(qo_indptr_host, kv_indptr_host, seq_lens_host,
+                                                  batch, num_heads, page_size, kv_dtype);
+    if (st != MLA_OK) return st;
+    const int sms = mla::device_sm_count();
+    if (sms <= 0) return MLA_ERR_CUDA;
+    Schedule s;
+    st = mla::build_extend_schedule(qo_indptr_host, kv_indptr_host, seq_lens_host, batch,
+                                    num_heads, page_size, kv_dtype, sms, s);
+    if (st != MLA_OK) return st;
+    return install(plan, std::move(s), workspace_bytes, stream);
 }
 
 extern "C" mla_status_t mla_decode_plan_destroy(mla_plan_t plan) {

@@ -20,8 +20,9 @@ constexpr int kTcTileTokens = 64;
 constexpr int kTcSegmentCost = 2;
 constexpr int kHeadsPerCta = 16;
 // tcgen05 path: per request, [q1;q2] as the shared-memory image the MMA reads
-// (2 x 16 rows x 576 E4M3, swizzled) followed by 16 fp32 score multipliers
-constexpr int kTcQImageBytes = 2 * kHeadsPerCta * 576 + kHeadsPerCta * 4;
+// (2 x 16 rows x 576 E4M3, swizzled) followed by 16 fp32 score multipliers and
+// 16 int32 causal limits (extend: a row sees the tokens before its limit)
+constexpr int kTcQImageBytes = 2 * kHeadsPerCta * 576 + kHeadsPerCta * 8;
 
 // Which decode kernel a plan launches.
 enum class DecodeKernel : int32_t {
@@ -44,16 +45,27 @@ struct Schedule {
     int32_t group_heads = 16;        // heads per CTA: 16, or 32 on the tcgen05 path when H % 32 == 0
     int32_t num_ctas = 0;            // token ranges; grid = num_ctas * head_groups
     std::vector<int32_t> cta_ptr;    // [num_ctas + 1] -> segment index
-    std::vector<int32_t> segs;       // 4 per segment: request, t0, t1, partial (-1 = final)
-    std::vector<int32_t> merge;      // 3 per entry: request, first partial, n partials
+    std::vector<int32_t> segs;       // 4 per segment: request (extend: query block), t0, t1,
+                                     // partial (-1 = final)
+    std::vector<int32_t> merge;      // 4 per entry: first output row, first partial,
+                                     // n partials, rows
+    int32_t part_rows = 0;           // rows per partial slot: H (decode), group_heads (extend)
     int32_t n_partials = 0;
+    // extend: the query rows (new token x head, row = token * H + head) of
+    // each request cut into blocks of group_heads rows; 4 ints per block:
+    // request, first row, rows, causal base (row r sees the tokens before
+    // base + r / H)
+    bool extend = false;
+    int32_t n_q = 0;                 // extend: query tokens (rows / H)
+    std::vector<int32_t> blocks;
     int64_t n_tokens = 0;
     size_t partial_lse_offset = 0;   // bytes into the workspace
     size_t qimg_offset = 0;          // tcgen05 path: q images, batch x kTcQImageBytes
     size_t workspace_bytes = 0;
 
     int32_t n_segs() const { return static_cast<int32_t>(segs.size() / 4); }
-    int32_t n_merge() const { return static_cast<int32_t>(merge.size() / 3); }
+    int32_t n_merge() const { return static_cast<int32_t>(merge.size() / 4); }
+    int32_t n_blocks() const { return static_cast<int32_t>(blocks.size() / 4); }
 };
 
 mla_status_t validate_plan_inputs(const int32_t* kv_indptr, const int32_t* seq_lens,
@@ -63,6 +75,15 @@ mla_status_t validate_plan_inputs(const int32_t* kv_indptr, const int32_t* seq_l
 mla_status_t build_schedule(const int32_t* kv_indptr, const int32_t* seq_lens, int32_t batch,
                             int32_t heads, int32_t page_size, mla_kv_dtype_t kv_dtype,
                             int32_t num_sms, Schedule& out);
+
+mla_status_t validate_extend_inputs(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                    const int32_t* seq_lens, int32_t batch, int32_t heads,
+                                    int32_t page_size, mla_kv_dtype_t kv_dtype);
+
+mla_status_t build_extend_schedule(const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                   const int32_t* seq_lens, int32_t batch, int32_t heads,
+                                   int32_t page_size, mla_kv_dtype_t kv_dtype, int32_t num_sms,
+                                   Schedule& out);
 
 }  // namespace mla
 
@@ -74,5 +95,5 @@ struct mla_plan {
     int32_t* pinned = nullptr;        // staging for the upload
     size_t pinned_cap = 0;
     cudaEvent_t upload_done = nullptr;
-    size_t off_cta = 0, off_segs = 0, off_merge = 0;   // element offsets in dev_meta
+    size_t off_cta = 0, off_segs = 0, off_merge = 0, off_blocks = 0;   // element offsets in dev_meta
 };

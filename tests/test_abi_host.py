@@ -12,8 +12,9 @@ import mla_decode_attention_run_gb300 as M
 import workloads as W
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mla_decode.h")
-# [q1;q2] as 2 x 16 rows of 576 E4M3 bytes, then 16 fp32 score multipliers
-QIMAGE_BYTES = 2 * 16 * 576 + 16 * 4
+# [q1;q2] as 2 x 16 rows of 576 E4M3 bytes, then 16 fp32 score multipliers and
+# 16 int32 causal limits
+QIMAGE_BYTES = 2 * 16 * 576 + 16 * 8
 SEGMENT_COST = 2          # tiles' worth of CTA time the tcgen05 schedule charges per segment
 
 

@@ -45,3 +45,13 @@ def test_decode_call_bytes_terms():
     assert A.decode_call_kv_bytes(lens) == 28_800
     assert A.decode_call_flops([1], heads=16) == 16 * 2176
     assert A.pages_of([1, 64, 65], 64) == 1 + 1 + 2
+
+
+def test_extend_counts():
+    # one new token per request is decode
+    assert A.extend_call_flops([17, 33], [1, 1], 4) == A.decode_call_flops([17, 33], 4)
+    # a 3-token prefill sees 1 + 2 + 3 tokens; 2 new tokens on a 5-token context see 4 + 5
+    assert A.extend_visible_tokens([3, 5], [3, 2]) == 6 + 9
+    # a request without new tokens moves nothing
+    b = A.extend_call_bytes([10, 7], [0, 2], heads=2, page_size=1)
+    assert b == 7 * 576 + 7 * 4 + 2 * 2 * (576 * 2 + 512 * 2 + 4) + (3 * 2 + 2) * 4

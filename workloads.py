@@ -21,6 +21,9 @@ Recipe (all draws with torch.Generator(seed = 1000 + config number), CPU):
   * slots: the first N_tok entries of a random permutation of the pool
     (page size 1), or a random permutation of the page ids (page size 64);
   * context lengths: fixed, or integers uniform in [1024, 8192] inclusive;
+  * extend steps: the context counts the request's new tokens (they are
+    stored before attention); their queries, [n_new, H, 576], are drawn with
+    the generator seeded 7919 above the workload's seed;
   * softmax_scale = 1/sqrt(192);
   * unused pool rows: random bytes other than the two NaN codes.
 """
@@ -149,6 +152,45 @@ def make_workload(name: str, *, batch: int | None = None, heads: int | None = No
                     seq_lens=seq, kv_indptr=kv_indptr, kv_indices=kv_indices,
                     q_bf16=_bf16_bits(q), latent_bf16=_bf16_bits(lat_bf16), latent_slots=slots,
                     k_scale=float(k_scale), seed=seed)
+
+
+# name -> (config number, B, H, contexts, new tokens per request): extend
+# steps.  The pages time the extend path's cast of the whole history (once
+# per layer and extend step) but give no chunk size; the readings here are a
+# prefill chunk of 256 new tokens over the decode workload's history law, and
+# 4 speculative tokens per request at the decode concurrency.
+EXTEND_CONFIGS = {
+    "extend_chunk": dict(base="concurrency", number=6, batch=8, q_len=256),
+    "spec_decode": dict(base="concurrency", number=7, batch=40, q_len=4),
+}
+
+
+def make_extend_workload(name: str, q_lens=None, **overrides) -> Workload:
+    """A seeded extend step: make_workload's page table and latents with
+    contexts that end in each request's new tokens, plus their queries.
+    name is an EXTEND_CONFIGS entry (its base config, batch and new-token
+    count) or a make_workload config (q_lens then required).  q_lens: one
+    count per request (or one for all), each <= its context.  Returns the
+    Workload with q_bf16 [n_new, H, 576] and extra["qo_indptr"] (int32 [B+1])."""
+    if name in EXTEND_CONFIGS:
+        ec = EXTEND_CONFIGS[name]
+        overrides.setdefault("batch", ec["batch"])
+        overrides.setdefault("seed", 1000 + ec["number"])
+        if q_lens is None:
+            q_lens = ec["q_len"]
+        name = ec["base"]
+    w = make_workload(name, **overrides)
+    B = w.batch
+    ql = np.broadcast_to(np.asarray(q_lens, np.int64), (B,)).astype(np.int32)
+    if np.any(ql < 0) or np.any(ql > w.seq_lens):
+        raise ValueError("each request's new tokens must fit in its context")
+    qo = np.zeros(B + 1, np.int32)
+    qo[1:] = np.cumsum(ql)
+    g = torch.Generator().manual_seed(w.seed + 7919)
+    q = torch.randn((int(qo[-1]), w.heads, D_ALL), generator=g, dtype=torch.float32)
+    w.q_bf16 = _bf16_bits(q)
+    w.extra["qo_indptr"] = qo
+    return w
 
 
 def decode_step_workload(batch: int, layers: int = NUM_LAYERS, seed: int = 1005,
