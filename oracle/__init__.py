@@ -56,6 +56,10 @@ def _load():
         lib.oracle_e4m3_encode_array.argtypes = [P, i64, P]
         lib.oracle_kv_store_fp8.argtypes = [P, P, P, i64, f32, P, i64, P, i64, i64]
         lib.oracle_kv_store_fp8.restype = i64
+        lib.oracle_kv_proj_fp8.argtypes = [P, P, i64, i32, P, f32, P, i64, P, i64, i64, P]
+        lib.oracle_kv_proj_fp8.restype = i64
+        lib.oracle_double_to_bf16.argtypes = [f64]
+        lib.oracle_double_to_bf16.restype = ctypes.c_uint16
         lib.oracle_kv_gather_cast.argtypes = [P, i64, P, i64, i64, P, i64, i32, f32, P, P]
         lib.oracle_kv_gather_cast.restype = i64
         dec_args = [P, P, i64, P, i64, i64, P, P, P, i32, i32, i32, f64, f64, P, P, P, i64,
@@ -124,6 +128,34 @@ def kv_store_fp8(ckv_new_bf16: np.ndarray, kpe_new_bf16: np.ndarray, slots: np.n
         _ptr(ckv), _ptr(kpe), _ptr(slots), n, np.float32(k_scale),
         ckv_pool.ctypes.data, ckv_pool.strides[0], kpe_pool.ctypes.data,
         kpe_pool.strides[0], ckv_pool.shape[0]))
+
+
+def double_to_bf16(x) -> np.ndarray:
+    """BF16 bits of float64 values rounded once to nearest, ties to even."""
+    lib = _load()
+    x = np.asarray(x, np.float64)
+    return np.array([lib.oracle_double_to_bf16(float(v)) for v in x.ravel()],
+                    np.uint16).reshape(x.shape)
+
+
+def kv_proj_fp8(x_bf16: np.ndarray, w_bf16: np.ndarray, slots: np.ndarray, k_scale: float,
+                ckv_pool: np.ndarray, kpe_pool: np.ndarray):
+    """KV projection + quantize-on-store.  x_bf16: uint16 [n, d]; w_bf16:
+    uint16 [576, d] (row j = weights of latent channel j); pools as for
+    kv_store_fp8 (written in place).  Returns (latent BF16 bits [n, 576],
+    number of out-of-range slots)."""
+    x = np.ascontiguousarray(x_bf16, np.uint16)
+    w = np.ascontiguousarray(w_bf16, np.uint16)
+    n, d = x.shape
+    assert w.shape == (D_ALL, d)
+    sl = np.ascontiguousarray(slots, np.int64)
+    assert sl.shape == (n,)
+    lat = np.zeros((n, D_ALL), np.uint16)
+    bad = _load().oracle_kv_proj_fp8(_ptr(x), _ptr(w), n, d, _ptr(sl), float(k_scale),
+                                     ckv_pool.ctypes.data, ckv_pool.strides[0],
+                                     kpe_pool.ctypes.data, kpe_pool.strides[0], ckv_pool.shape[0],
+                                     _ptr(lat))
+    return lat, int(bad)
 
 
 def kv_gather_cast(ckv_pool: np.ndarray, kpe_pool: np.ndarray, kv_indices: np.ndarray,

@@ -159,6 +159,74 @@ int64_t oracle_kv_store_fp8(const uint16_t* ckv_new, const uint16_t* kpe_new,
     return bad;
 }
 
+/* ------------------------------------------- fused KV projection store */
+
+/* Round a double to the nearest BF16 value, ties to even (one rounding of
+ * the double itself, not through float).  BF16: 8 significant bits, the
+ * float exponent range, subnormal spacing 2^-133; beyond the largest finite
+ * value (2^128 - 2^120) the result is +-inf. */
+static uint16_t double_to_bf16_rne(double x) {
+    if (x != x) return 0x7FC0;
+    if (x == 0.0) return signbit(x) ? 0x8000 : 0x0000;
+    int e = 0;
+    frexp(x, &e);                       /* |x| = m * 2^e, m in [0.5, 1) */
+    int q = e - 8;                      /* spacing of 8-bit significands */
+    if (q < -133) q = -133;             /* subnormal spacing */
+    double r = nearbyint(ldexp(x, -q)); /* default rounding: nearest, ties even */
+    double v = ldexp(r, q);
+    if (fabs(v) >= ldexp(1.0, 128)) return signbit(x) ? 0xFF80 : 0x7F80;
+    float f = (float)v;                 /* exact: v has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+uint16_t oracle_double_to_bf16(double x) { return double_to_bf16_rne(x); }
+
+/* The KV projection with the cache write fused into it ([P1] "Step 3",
+ * CastToFP8: every step's new KV comes out of the attention projection in
+ * BF16 and set_kv_buffer quantizes it into the FP8 cache as a separate copy;
+ * "From Attribution to Optimization Targets": the projection kernel should
+ * emit FP8 itself).  The pages give neither the projection's shape nor its
+ * weights; the reading: one linear map of the hidden state to the 576 latent
+ * channels (512 c_kv, then 64 k_pe), weights w[j][k] for output channel j,
+ * whose BF16 output is what the unfused path stores:
+ *   latent[i][j] = BF16_rne( sum_k x[i][k] * w[j][k] )   (exact sum, one rounding)
+ *   pool rows slots[i] = kv_store_fp8(latent[i])          (as above)
+ * The products of BF16 values are exact in double and the sums of up to a
+ * few thousand of them carry far more than the 8 bits the rounding keeps.
+ * x: BF16 [n][d], w: BF16 [576][d]; latent_out (optional): BF16 [n][576].
+ * Returns the number of out-of-range slots (their rows are left alone). */
+int64_t oracle_kv_proj_fp8(const uint16_t* x, const uint16_t* w, int64_t n, int32_t d,
+                           const int64_t* slots, float k_scale, uint8_t* ckv_pool,
+                           int64_t ckv_stride, uint8_t* kpe_pool, int64_t kpe_stride,
+                           int64_t num_slots, uint16_t* latent_out) {
+    uint16_t* lat = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * D_ALL);
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        for (int j = 0; j < D_ALL; ++j) {
+            double acc = 0.0;
+            for (int32_t k = 0; k < d; ++k)
+                acc += (double)bf16_to_float(x[i * d + k]) * (double)bf16_to_float(w[(int64_t)j * d + k]);
+            lat[i * D_ALL + j] = double_to_bf16_rne(acc);
+        }
+    }
+    if (latent_out) memcpy(latent_out, lat, sizeof(uint16_t) * (size_t)n * D_ALL);
+    /* the store reads c_kv and k_pe as separate [n][512] / [n][64] arrays */
+    uint16_t* ckv = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * D_CKV);
+    uint16_t* kpe = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(n > 0 ? n : 1) * D_KPE);
+    for (int64_t i = 0; i < n; ++i) {
+        memcpy(ckv + i * D_CKV, lat + i * D_ALL, sizeof(uint16_t) * D_CKV);
+        memcpy(kpe + i * D_KPE, lat + i * D_ALL + D_CKV, sizeof(uint16_t) * D_KPE);
+    }
+    int64_t bad = oracle_kv_store_fp8(ckv, kpe, slots, n, k_scale, ckv_pool, ckv_stride,
+                                      kpe_pool, kpe_stride, num_slots);
+    free(lat);
+    free(ckv);
+    free(kpe);
+    return bad;
+}
+
 /* -------------------------------------------------------- gather-cast */
 
 /* Gather-then-cast ([P3] "The Reasoning Process"): the rows of the listed
