@@ -414,6 +414,7 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_configs:
         result["configs"] = measure_configs(torch, M, dev, stream)
         result["extend"] = measure_extend(torch, M, dev, stream)
+        result["kv_proj"] = measure_kv_proj(torch, M, dev, stream)
 
     # ---- CPU oracle baseline (rank 0, one GPU)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -570,6 +571,74 @@ def measure_extend(torch, M, dev, stream, n_pools=8):
         M.mla_decode_plan_destroy(plan)
         del q, out, lse, ws, ckv_c, kpe_c
     del pools
+    torch.cuda.empty_cache()
+    return res
+
+
+# Hidden size of the projection's input.  The pages do not give it; this is
+# the hidden size of the DeepSeek-V3 family that Kimi-K2.5 belongs to.
+PROJ_D_MODEL = 7168
+
+
+def measure_kv_proj(torch, M, dev, stream, batch=40, layers=W.NUM_LAYERS, d_model=PROJ_D_MODEL):
+    """The decode step's KV write with the projection: per layer, batch new
+    tokens' hidden states [batch, d_model] times that layer's weights
+    [576, d_model] into the latent, stored as E4M3 into the pool.  Fused:
+    kv_proj_store_fp8 (one kernel).  Unfused: cuBLAS BF16 GEMMs (torch.matmul)
+    to the BF16 c_kv and k_pe latents, then kv_store_fp8.  Each is a CUDA graph over all
+    layers (the layers' weights, 0.64 GB, are far larger than L2)."""
+    peak, _ = measured_peaks()
+    g = torch.Generator(device=dev).manual_seed(77)
+    P = W.POOL_SLOTS
+    pool = torch.empty((P, W.D_ALL), dtype=torch.uint8, device=dev)
+    k_scale = latent_pool_(torch, pool, seed=78)
+    x = torch.randn(layers, batch, d_model, generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn(layers, W.D_ALL, d_model, generator=g, device=dev) / math.sqrt(d_model)).to(
+        torch.bfloat16)
+    slots = torch.randperm(P, generator=g, device=dev)[:batch].to(torch.int64)
+    lat_ckv = torch.empty(layers, batch, 512, dtype=torch.bfloat16, device=dev)
+    lat_kpe = torch.empty(layers, batch, 64, dtype=torch.bfloat16, device=dev)
+
+    def fused(l, s):
+        M.kv_proj_store_fp8(x[l], w[l], slots, k_scale, pool[:, :512], pool[:, 512:], stream=s)
+
+    def unfused(l, s):
+        # the store takes c_kv and k_pe as separate contiguous arrays
+        torch.matmul(x[l], w[l, :512].t(), out=lat_ckv[l])
+        torch.matmul(x[l], w[l, 512:].t(), out=lat_kpe[l])
+        M.kv_store_fp8(lat_ckv[l], lat_kpe[l], slots, k_scale, pool[:, :512], pool[:, 512:],
+                       stream=s)
+
+    def time_graph(fn):
+        with torch.cuda.stream(stream):
+            for l in range(layers):
+                fn(l, stream)
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for l in range(layers):
+                fn(l, torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            gr.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / (5 * layers)
+
+    us_fused = time_graph(fused)
+    us_unfused = time_graph(unfused)
+    nbytes = A.kv_proj_bytes(batch, d_model)
+    res = {"batch": batch, "d_model": d_model, "layers": layers,
+           "fused_us_per_layer": round(us_fused, 3), "unfused_us_per_layer": round(us_unfused, 3),
+           "unfused": "cuBLAS BF16 GEMMs (torch.matmul: c_kv and k_pe outputs) + kv_store_fp8",
+           "achieved_gbs": round(nbytes / us_fused / 1e3, 1),
+           "hbm_frac": round(nbytes / us_fused / 1e3 / peak, 4),
+           "bytes_per_layer": nbytes, "d_model_source": "DeepSeek-V3 family hidden size (not on the pages)"}
+    del pool, x, w, lat_ckv, lat_kpe
     torch.cuda.empty_cache()
     return res
 
@@ -735,12 +804,26 @@ def main(argv=None):
     ap.add_argument("--extend-only", action="store_true",
                     help="time only the extend workloads and print their JSON (a diagnostic, "
                          "not the benchmark line)")
+    ap.add_argument("--proj-only", action="store_true",
+                    help="time only the fused KV projection store against cuBLAS + store and "
+                         "print its JSON (a diagnostic)")
     ap.add_argument("--pools", type=int, default=8,
                     help="pools the extend timing rotates over (--extend-only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_env()
+    if args.proj_only:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        import mla_decode_attention_run_gb300 as M
+        torch.cuda.set_device(local)
+        stream = torch.cuda.Stream()
+        res = measure_kv_proj(torch, M, torch.device("cuda", local), stream, layers=args.layers)
+        if rank == 0:
+            print(json.dumps({"kv_proj": res}), flush=True)
+        return
     if args.extend_only:
         import torch
         import __graft_entry__

@@ -321,6 +321,39 @@ mla_status_t kv_store_fp8(const void* ckv_new, const void* kpe_new,
                           int64_t num_pool_slots, void* stream);
 
 /*
+ * kv_proj_store_fp8 -- the KV projection with the FP8 cache write fused into
+ * its epilogue ([P1] "Step 3", CastToFP8: the new BF16 KV comes out of the
+ * attention projection and set_kv_buffer quantizes it as a separate copy;
+ * [P1] "From Attribution to Optimization Targets": let the projection
+ * kernel emit FP8 directly).  The pages give no shape for the projection;
+ * the reading implemented: one linear map of each new token's hidden state
+ * to the 576 latent channels (512 c_kv, then 64 k_pe),
+ *     latent[i][j] = BF16_rne( sum_k x[i][k] * w[j][k] )   (fp32 accumulation)
+ * and then, per token, exactly kv_store_fp8 of that BF16 row into pool row
+ * slots[i].  One kernel: BF16 tensor-core GEMM, rounding, quantization and
+ * scatter; no BF16 latent is written unless latent_out is given.
+ *  x           BF16 [n][d_model], row stride x_row_stride elements (a multiple
+ *              of 8, >= d_model), 16-byte aligned.
+ *  w           BF16 [576][d_model]: row j holds the weights of latent channel
+ *              j (the transposed weight matrix), row stride w_row_stride.
+ *  d_model     a multiple of 64, 64 .. 65536.
+ *  slots       int64 [n], device; an out-of-range slot skips its row and
+ *              sets MLA_FLAG_INDEX_OOB.  Duplicate slots give an unspecified row.
+ *  k_scale, pools, num_pool_slots   as for kv_store_fp8.
+ *  latent_out  optional BF16 [n][576], contiguous, 16-byte aligned: the
+ *              rounded latents the bytes were made from.
+ * n = 0 is a no-op.  Asynchronous on `stream`; no allocation, no workspace.
+ * Errors: MLA_ERR_INVALID_ARG (NULL / bad size / scale), MLA_ERR_UNSUPPORTED
+ * (alignment), MLA_ERR_CUDA (launch).
+ */
+mla_status_t kv_proj_store_fp8(const void* x, int64_t x_row_stride, const void* w,
+                               int64_t w_row_stride, int64_t n, int32_t d_model,
+                               const int64_t* slots, float k_scale, void* ckv_pool,
+                               int64_t ckv_row_stride_bytes, void* kpe_pool,
+                               int64_t kpe_row_stride_bytes, int64_t num_pool_slots,
+                               void* latent_out, void* stream);
+
+/*
  * kv_gather_cast -- gather-then-cast of the active pages ([P3] "The
  * Reasoning Process"): row j*page_size + r of the outputs is pool slot
  * kv_indices[j]*page_size + r, converted as

@@ -19,6 +19,7 @@ __all__ = [
     "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast", "mla_get_last_error",
     "exported_symbols", "D_CKV", "D_KPE", "D_QK", "mla_decode_run_static_scratch",
     "STATIC_SCRATCH_BYTES", "mla_extend_plan", "mla_extend_run", "mla_extend_schedule",
+    "kv_proj_store_fp8",
 ]
 
 D_CKV, D_KPE, D_QK = 512, 64, 576
@@ -68,6 +69,8 @@ def library():
     lib.mla_extend_schedule.argtypes = [_P, _P, _P, _i32, _i32, _i32, ctypes.c_int, _i32, _P, _i32,
                                         _P, _i32, _P, ctypes.POINTER(_sz)]
     lib.kv_store_fp8.argtypes = [_P, _P, _P, _i64, _f32, _P, _i64, _P, _i64, _i64, _P]
+    lib.kv_proj_store_fp8.argtypes = [_P, _i64, _P, _i64, _i64, _i32, _P, _f32, _P, _i64, _P, _i64,
+                                      _i64, _P, _P]
     lib.kv_gather_cast.argtypes = [_P, _i64, _P, _i64, _i64, _P, _i64, _i32, _f32, _P, _P, _P]
     lib.mla_get_last_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -75,7 +78,7 @@ def library():
     for name in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
                  "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
                  "mla_get_last_error", "mla_decode_run_static_scratch", "mla_extend_plan",
-                 "mla_extend_run", "mla_extend_schedule"):
+                 "mla_extend_run", "mla_extend_schedule", "kv_proj_store_fp8"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -89,7 +92,7 @@ def exported_symbols() -> list[str]:
     for n in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
               "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
               "mla_get_last_error", "mla_status_string", "mla_decode_run_static_scratch",
-              "mla_extend_plan", "mla_extend_run", "mla_extend_schedule"):
+              "mla_extend_plan", "mla_extend_run", "mla_extend_schedule", "kv_proj_store_fp8"):
         getattr(lib, n)
         names.append(n)
     return names
@@ -286,6 +289,21 @@ def kv_store_fp8(ckv_new, kpe_new, slots, k_scale: float, ckv_pool, kpe_pool,
                                   k_scale, ckv_pool.data_ptr(), _row_stride_bytes(ckv_pool),
                                   kpe_pool.data_ptr(), _row_stride_bytes(kpe_pool), nps,
                                   _stream(stream)), "kv_store_fp8")
+
+
+def kv_proj_store_fp8(x, w, slots, k_scale: float, ckv_pool, kpe_pool,
+                      num_pool_slots: int | None = None, latent_out=None, stream=None):
+    """x bf16 [n, d_model], w bf16 [576, d_model] (row j = channel j's
+    weights), slots int64 [n]: latent = BF16(x @ w.T) quantized into the pool
+    rows like kv_store_fp8; latent_out (optional) bf16 [n, 576] receives the
+    rounded latents."""
+    n, d = x.shape
+    nps = ckv_pool.shape[0] if num_pool_slots is None else num_pool_slots
+    _check(library().kv_proj_store_fp8(x.data_ptr(), x.stride(0), w.data_ptr(), w.stride(0), n, d,
+                                       slots.data_ptr(), k_scale, ckv_pool.data_ptr(),
+                                       _row_stride_bytes(ckv_pool), kpe_pool.data_ptr(),
+                                       _row_stride_bytes(kpe_pool), nps, _dptr(latent_out),
+                                       _stream(stream)), "kv_proj_store_fp8")
 
 
 def kv_gather_cast(ckv_pool, kpe_pool, kv_indices, page_size: int, k_scale: float, ckv_out,

@@ -69,6 +69,12 @@ def extend_call_flops(seq_lens, q_lens, heads: int) -> int:
     return int(extend_visible_tokens(seq_lens, q_lens) * heads * 2 * (D_QK + D_CKV))
 
 
+def kv_proj_bytes(n_tokens: int, d_model: int) -> int:
+    """Fused projection + store: the weights [576, d_model] and the hidden
+    states [n, d_model] in BF16, the E4M3 rows and the slots out."""
+    return int(D_QK * d_model * 2 + n_tokens * d_model * 2 + n_tokens * (D_QK + 8))
+
+
 def store_bytes(n_tokens: int) -> int:
     """Quantize-on-store: BF16 rows in (2 B/element), E4M3 rows out, slots."""
     return int(n_tokens * (D_QK * 2 + D_QK + 8))

@@ -19,7 +19,7 @@ BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmla_decode.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["runtime.cu", "kv_cache.cu", "plan.cu", "decode.cu", "decode_tc.cu",
-           "decode_static.cu"]
+           "decode_static.cu", "kv_proj.cu"]
 
 
 def _nvcc() -> str:

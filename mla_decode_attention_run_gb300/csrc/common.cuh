@@ -92,6 +92,20 @@ MLA_DEVINLINE uint16_t f32x2_to_e4m3x2(float first, float second) {
     return r;
 }
 
+// Quantize-on-store of two BF16 values (one 32-bit word, first value in the
+// low half): each is widened exactly to fp32, divided by k_scale in one IEEE
+// division and rounded to E4M3 (nearest even, saturating; NaN -> 0x7F).
+// Returns the first byte in the low byte.
+MLA_DEVINLINE uint16_t bf16x2_to_e4m3x2_scaled(uint32_t word, float k_scale) {
+    const float a = __fdiv_rn(__uint_as_float(word << 16), k_scale);
+    const float b = __fdiv_rn(__uint_as_float(word & 0xFFFF0000u), k_scale);
+    uint16_t two = f32x2_to_e4m3x2(a, b);
+    // NaN encodes as the canonical 0x7F whatever its sign
+    if (a != a) two = static_cast<uint16_t>((two & 0xFF00u) | 0x7Fu);
+    if (b != b) two = static_cast<uint16_t>((two & 0x00FFu) | 0x7F00u);
+    return two;
+}
+
 MLA_DEVINLINE uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));

@@ -15,11 +15,6 @@ namespace {
 constexpr int kStoreUnitsPerRow = (kDCkv + kDKpe) / 8;   // 8 elements per thread
 constexpr int kGatherUnitsPerRow = (kDCkv + kDKpe) / 16; // 16 bytes per thread
 
-// BF16 value divided by k_scale: exact widening, then one IEEE fp32 division.
-__device__ __forceinline__ float scaled_latent(uint16_t bf16_bits, float k_scale) {
-    return __fdiv_rn(__uint_as_float(static_cast<uint32_t>(bf16_bits) << 16), k_scale);
-}
-
 __global__ void __launch_bounds__(256)
 kv_store_fp8_kernel(const uint16_t* __restrict__ ckv_new, const uint16_t* __restrict__ kpe_new,
                     const int64_t* __restrict__ slots, int64_t n, float k_scale,
@@ -52,16 +47,8 @@ kv_store_fp8_kernel(const uint16_t* __restrict__ ckv_new, const uint16_t* __rest
         for (int p = 0; p < 2; ++p) {
             uint32_t bytes = 0;
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const uint32_t word = w[2 * p + q];
-                const float a = scaled_latent(static_cast<uint16_t>(word & 0xFFFFu), k_scale);
-                const float b = scaled_latent(static_cast<uint16_t>(word >> 16), k_scale);
-                uint16_t two = f32x2_to_e4m3x2(a, b);
-                // NaN encodes as the canonical 0x7F whatever its sign
-                if (a != a) two = static_cast<uint16_t>((two & 0xFF00u) | 0x7Fu);
-                if (b != b) two = static_cast<uint16_t>((two & 0x00FFu) | 0x7F00u);
-                bytes |= static_cast<uint32_t>(two) << (16 * q);
-            }
+            for (int q = 0; q < 2; ++q)
+                bytes |= static_cast<uint32_t>(bf16x2_to_e4m3x2_scaled(w[2 * p + q], k_scale)) << (16 * q);
             packed[p] = bytes;
         }
         *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);

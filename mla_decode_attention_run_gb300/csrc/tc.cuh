@@ -47,6 +47,14 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, b
            | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f16 with BF16 x BF16 -> F32, both operands
+// K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+    return (1u << 4)                                  // D format: F32
+           | (1u << 7) | (1u << 10)                   // A, B format: BF16
+           | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // ------------------------------------------------------------------ tcgen05
 
 MLA_DEVINLINE void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
@@ -64,6 +72,15 @@ MLA_DEVINLINE void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, u
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n"
+        :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
+MLA_DEVINLINE void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                            bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
         :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
         : "memory");
 }
@@ -171,6 +188,32 @@ MLA_DEVINLINE void prefetch_row_l2(const void* row) {
     // the line of the row's last byte (beyond the loop's lines when the row
     // starts past the middle of a line)
     asm volatile("prefetch.global.L2 [%0];\n" :: "l"(r + kBytes - 1));
+}
+
+// ----------------------------------------------------------------- clusters
+
+MLA_DEVINLINE uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// All threads of all CTAs of the cluster meet; shared-memory writes made
+// before it are visible to every CTA of the cluster after it.
+MLA_DEVINLINE void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// The address of the same shared-memory variable in CTA `rank` of the cluster.
+MLA_DEVINLINE uint32_t cluster_map(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+MLA_DEVINLINE float4 ld_cluster_f4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 MLA_DEVINLINE uint64_t global_ns() {

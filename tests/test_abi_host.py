@@ -204,3 +204,16 @@ def test_entry_points_reject_null_and_accept_empty_without_cuda():
     assert lib.mla_decode_run(None, 16, 0, 576, 16, 576, 16, 576, 10, 16, 16, 16, 1.0, 0.07, 16,
                               16, None, 0, None) == 1
     assert M.library().mla_decode_plan_destroy(None) == 0
+    # fused projection store: n = 0 is a no-op; bad sizes, scale and alignment
+    assert lib.kv_proj_store_fp8(None, 64, None, 64, 0, 64, None, 1.0, None, 576, None, 576, 10,
+                                 None, None) == 0
+    assert lib.kv_proj_store_fp8(16, 64, 16, 64, -1, 64, 16, 1.0, 16, 576, 16, 576, 10, None,
+                                 None) == 1
+    assert lib.kv_proj_store_fp8(16, 96, 16, 96, 3, 96, 16, 1.0, 16, 576, 16, 576, 10, None,
+                                 None) == 1                       # d_model not a multiple of 64
+    assert lib.kv_proj_store_fp8(16, 64, 16, 64, 3, 64, 16, 0.0, 16, 576, 16, 576, 10, None,
+                                 None) == 1
+    assert lib.kv_proj_store_fp8(17, 64, 16, 64, 3, 64, 16, 1.0, 16, 576, 16, 576, 10, None,
+                                 None) == 2                       # misaligned x
+    assert lib.kv_proj_store_fp8(16, 64, 16, 64, 3, 64, 16, 1.0, 16, 576, 16, 576, 10, 24,
+                                 None) == 2                       # misaligned latent_out
