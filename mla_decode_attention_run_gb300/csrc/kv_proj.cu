@@ -13,16 +13,18 @@
 // (128-byte) chunks through a 6-stage cp.async ring, 128-byte swizzle.  The
 // weights are the bytes that matter when few tokens come in (a decode step:
 // 576 x d_model BF16 per layer), so K is split over a thread-block cluster
-// of up to 8 CTAs, as wide as still lets every cluster run at once; each CTA
-// leaves its fp32 partial tile in shared memory (token rows past the batch
-// are zeroed once, not loaded);
-// after a cluster barrier CTA r sums rows r, r + S, ... across the cluster
-// (distributed shared memory), rounds, quantizes and stores them.
-// No workspace, no second launch.
+// of up to 16 CTAs, as wide as still lets every cluster run at once.  Row r
+// of the tile belongs to CTA r mod S of the cluster: every CTA writes its
+// fp32 partial of row r straight into that CTA's shared memory (distributed
+// shared memory), and after one cluster barrier each CTA sums its rows'
+// partials in a fixed order (deterministic), rounds, quantizes and stores
+// them.  Token rows past the batch are never loaded: warps 3-5 zero them
+// once per stage buffer while the first loads are in flight.  No workspace,
+// no second launch.
 //
 // Warps: 0-1 load, lane 0 of warp 2 issues the MMAs, warps 2-5 (one per TMEM
 // lane quadrant) read the accumulator out.  Waits are bounded; after a
-// timeout the CTA still reaches both cluster barriers, so no CTA of its
+// timeout the CTA still reaches the cluster barrier, so no CTA of its
 // cluster waits forever.
 #include <cmath>
 #include <mutex>
@@ -40,7 +42,7 @@ constexpr int kPM = 128;                     // token rows per tile (MMA M)
 constexpr int kPK = 64;                      // K elements per stage: one 128-byte row
 constexpr int kPLoadWarps = 2;
 constexpr int kPThreads = 192;
-constexpr int kPMaxSplit = 8;                // portable cluster size
+constexpr int kPMaxSplit = 16;               // cluster size (8 is portable; 16 where allowed)
 constexpr int kATile = kPM * 128;            // 16 KB
 
 // Shared-memory map for N latent channels per tile.
@@ -51,8 +53,10 @@ struct ProjShape {
     static constexpr int kStages = N == 32 ? 8 : 6;
     static constexpr int kRedStride = N + 4;            // floats per partial-tile row (spreads banks)
     static constexpr int kOffRed = kStages * kStage;
-    static constexpr int kOffBar = kOffRed + kPM * kRedStride * 4;
-    static constexpr int kNumBars = 2 * kStages + 1;    // full[], empty[], done
+    // partial rows received from the cluster: split x ceil(128 / split) rows
+    static constexpr int kRedRows = kPM + kPMaxSplit;
+    static constexpr int kOffBar = kOffRed + kRedRows * kRedStride * 4;
+    static constexpr int kNumBars = 2 * kStages + 2;    // full[], empty[], done, zero
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmem = kOffMisc + 16 + 1024;
     static constexpr uint32_t kTmemCols = N;
@@ -84,7 +88,7 @@ template <int N>
 __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjParams p) {
     using S = ProjShape<N>;
     constexpr int kStages = S::kStages;
-    constexpr int FULL = 0, EMPTY = kStages, DONE = 2 * kStages;
+    constexpr int FULL = 0, EMPTY = kStages, DONE = 2 * kStages, ZERO = 2 * kStages + 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + S::kOffBar);
@@ -106,17 +110,10 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
             mbar_init(&bars[EMPTY + s], 1);
         }
         mbar_init(&bars[DONE], 1);
+        mbar_init(&bars[ZERO], 96);
         *abort = 0;
         mbar_fence_init();
     }
-    // token rows past the batch: zero in every stage, once (the loads skip them)
-    for (int q = rows * 8 + tid; q < kPM * 8; q += kPThreads) {
-        const int r = q >> 3, c = q & 7;
-#pragma unroll 1
-        for (int s = 0; s < kStages; ++s)
-            *reinterpret_cast<uint4*>(base + s * S::kStage + r * 128 + ((c ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-    }
-    fence_proxy_async_smem();                     // visible to the tensor core's reads
     if (warp == 2) tmem_alloc(tmem_slot, S::kTmemCols);
     fence_before_sync();
     __syncthreads();
@@ -145,9 +142,12 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
             mbar_arrive_cp_async(&bars[FULL + s]);
         }
         cp_async_wait<0>();
-    } else if (warp == 2 && lane == 0) {
+    } else if (warp == 2) {
+        if (lane == 0) {
         const uint32_t idesc = idesc_bf16_f32(kPM, N);
-        for (int i = 0; i < nch; ++i) {
+        // the zeroed rows must be in place before the first MMA reads them
+        const bool zeroed = mbar_wait(&bars[ZERO], 0, abort, p.flags);
+        for (int i = 0; zeroed && i < nch; ++i) {
             const int s = i % kStages;
             const uint32_t u = static_cast<uint32_t>(i / kStages);
             if (!mbar_wait(&bars[FULL + s], u & 1, abort, p.flags)) break;
@@ -163,44 +163,62 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
             mma_commit(&bars[EMPTY + s]);                 // the stage may be refilled
         }
         mma_commit(&bars[DONE]);                          // every MMA issued has completed
+        }
+    } else {
+        // warps 3-5: token rows past the batch, zero in every stage, once
+        for (int q = rows * 8 + (tid - 96); q < kPM * 8; q += 96) {
+            const int r = q >> 3, c = q & 7;
+#pragma unroll 1
+            for (int s = 0; s < kStages; ++s)
+                *reinterpret_cast<uint4*>(base + s * S::kStage + r * 128 + ((c ^ (r & 7)) << 4)) =
+                    make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();                         // visible to the tensor core's reads
+        mbar_arrive(&bars[ZERO]);
     }
     __syncwarp();
 
-    // the partial tile (this CTA's K range) to shared memory: row = TMEM lane
+    // this CTA's partial of tile row r (= TMEM lane) goes to CTA r mod S of
+    // the cluster, partial slot [rank][r / S]
+    const int rpo = (kPM + split - 1) / split;            // rows per owning CTA
     if (warp >= 2) {
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const bool ok = mbar_wait(&bars[DONE], 0, abort, p.flags);
         fence_after_sync();
-        float* dst = red + row * S::kRedStride;
+        const uint32_t dst = cluster_map(smem_u32(red + (rank * rpo + row / split) * S::kRedStride),
+                                         static_cast<uint32_t>(row % split));
 #pragma unroll
         for (int c = 0; c < N; c += 16) {
             uint32_t r[16];
             tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, r);
             tmem_wait_ld();
+            if (row < rows) {
 #pragma unroll
-            for (int e = 0; e < 16; e += 4)
-                *reinterpret_cast<float4*>(dst + c + e) =
-                    ok ? make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]), __uint_as_float(r[e + 2]),
-                                     __uint_as_float(r[e + 3]))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int e = 0; e < 16; e += 4)
+                    st_cluster_f4(dst + 4 * (c + e),
+                                  ok ? make_float4(__uint_as_float(r[e]), __uint_as_float(r[e + 1]),
+                                                   __uint_as_float(r[e + 2]), __uint_as_float(r[e + 3]))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f));
+            }
         }
     }
     fence_before_sync();
     __syncthreads();
-    cluster_sync();                                       // every CTA's partial tile is written
+    cluster_sync();                                       // every partial row has arrived
 
-    // rows rank, rank + S, ...: sum the S partials, round to BF16, quantize, store
+    // rows rank, rank + S, ...: sum the S partials (in rank order), round to
+    // BF16, quantize, store
     if (warp >= 2) {
         constexpr int kChunks = N / 4;                    // float4 per row
         constexpr int kRowsPerPass = 128 / kChunks;
         const int t = tid - 64;                           // 0..127
         const int c4 = t % kChunks;
-        for (int r = rank + split * (t / kChunks); r < rows; r += split * kRowsPerPass) {
-            const uint32_t local = smem_u32(red + r * S::kRedStride + 4 * c4);
-            float4 acc = ld_cluster_f4(cluster_map(local, 0));
+        for (int lr = t / kChunks; rank + lr * split < rows; lr += kRowsPerPass) {
+            const int r = rank + lr * split;
+            float4 acc = *reinterpret_cast<const float4*>(red + lr * S::kRedStride + 4 * c4);
             for (int src = 1; src < split; ++src) {
-                const float4 v = ld_cluster_f4(cluster_map(local, static_cast<uint32_t>(src)));
+                const float4 v = *reinterpret_cast<const float4*>(red + (src * rpo + lr) * S::kRedStride + 4 * c4);
                 acc.x += v.x;
                 acc.y += v.y;
                 acc.z += v.z;
@@ -221,12 +239,13 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
             *reinterpret_cast<uint32_t*>(dst + 4 * c4) = bytes;
         }
     }
-    cluster_sync();                                       // no CTA leaves while its tile is read
+    // no CTA touches another's shared memory after the barrier: nobody waits
     if (warp == 2) tmem_dealloc(tmem, S::kTmemCols);
 }
 
 std::mutex g_proj_mu;
-std::vector<char> g_proj_attr;      // per device: bit (N / 32 - 1): max dynamic shared memory set
+std::vector<char> g_proj_attr;      // per device: bit (N / 32 - 1): attributes set
+std::vector<int> g_proj_max_split;  // per device: widest cluster the device accepts
 std::vector<std::vector<int>> g_proj_fit;   // per device, per split: clusters that fit at once
 
 template <int N>
@@ -240,13 +259,21 @@ mla_status_t launch_proj(const ProjParams& p, int64_t m_tiles, int dev, cudaStre
             if (cudaFuncSetAttribute(kv_proj_store_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      S::kSmem) != cudaSuccess)
                 return MLA_ERR_CUDA;
+            if ((int)g_proj_max_split.size() <= dev) g_proj_max_split.resize(dev + 1, 8);
+            // clusters of 16 are not portable: use them where the device allows
+            g_proj_max_split[dev] =
+                cudaFuncSetAttribute(kv_proj_store_kernel<N>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                        cudaSuccess
+                    ? kPMaxSplit
+                    : 8;
+            cudaGetLastError();
             g_proj_attr[dev] |= bit;
         }
     }
-    // split K over the widest cluster (up to 8 CTAs) whose clusters all fit
+    // split K over the widest cluster (up to 16 CTAs) whose clusters all fit
     // on the GPU at once: a second wave of clusters costs more than a
-    // narrower split (measured on GB300 at 40 tokens: split 8 over 9 tiles
-    // 9.8 us, 32-channel tiles split 8, two waves, 17.3 us)
+    // narrower split (measured on GB300 at 40 tokens: 9 tiles split 16
+    // 8.3 us, split 8 8.9 us; 32-channel tiles split 8, two waves, 17.3 us)
     const int64_t tiles = m_tiles * (kDQk / N);
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kPThreads);
@@ -259,7 +286,12 @@ mla_status_t launch_proj(const ProjParams& p, int64_t m_tiles, int dev, cudaStre
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int split = 1;
-    for (int s = kPMaxSplit < p.kchunks ? kPMaxSplit : p.kchunks; s > 1; --s) {
+    int max_split = 8;
+    {
+        std::lock_guard<std::mutex> lk(g_proj_mu);
+        max_split = g_proj_max_split[dev];
+    }
+    for (int s = max_split < p.kchunks ? max_split : p.kchunks; s > 1; --s) {
         if (tiles * s > device_sm_count()) continue;
         cfg.gridDim = dim3(static_cast<unsigned>(s), kDQk / N, static_cast<unsigned>(m_tiles));
         attr[0].val.clusterDim.x = static_cast<unsigned>(s);

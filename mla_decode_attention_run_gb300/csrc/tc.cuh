@@ -216,6 +216,11 @@ MLA_DEVINLINE float4 ld_cluster_f4(uint32_t cluster_addr) {
     return v;
 }
 
+MLA_DEVINLINE void st_cluster_f4(uint32_t cluster_addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n"
+                 :: "r"(cluster_addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w) : "memory");
+}
+
 MLA_DEVINLINE uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
