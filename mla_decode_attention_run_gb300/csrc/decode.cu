@@ -382,69 +382,69 @@ __global__ void __launch_bounds__(kThreads, 1) mla_decode_mma_kernel(const Decod
     }
 }
 
-// Combine split-KV partials: one warp per output row (request x head, or a
-// query block's row); lane i holds the lse of partial i (per 32-partial
-// chunk), the max and the weight sum are warp-shuffle reductions, and each
-// lane accumulates 16 output channels.  Entry e: output rows row0 .. row0 +
-// rows - 1 from partials first .. first + n - 1, row h of each at partial
-// row h (part_rows rows per partial).
+// Combine split-KV partials.  One block of 128 threads per output row
+// (request x head, or a query block's row), thread t owning channels
+// 4t .. 4t + 3.  Entry e: output rows row0 .. row0 + rows - 1 from partials
+// first .. first + n - 1, row h of each at partial row h (part_rows rows per
+// partial).  Partials are taken eight at a time (their lse and o loads all
+// in flight together), folded in with a running maximum:
+//   m' = max(m, max_i lse_i);  acc = acc * e^(m - m') + sum_i e^(lse_i - m') o_i
+// so a request split into n partials costs about n / 8 memory round trips.
+constexpr int kMergeBatch = 8;
+
 __global__ void __launch_bounds__(128)
 mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int part_rows,
                  const float* __restrict__ part_o, const float* __restrict__ part_lse,
                  uint16_t* __restrict__ out, float* __restrict__ lse) {
     griddep_wait();                                 // the decode kernel's partials are complete
-    const int e = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = blockIdx.y * 4 + warp;
+    const int e = blockIdx.x, h = blockIdx.y, t = threadIdx.x;
     if (e >= n_merge) return;
     const int row0 = merge[4 * e], first = merge[4 * e + 1], n = merge[4 * e + 2], rows = merge[4 * e + 3];
     if (h >= rows) return;
     const int64_t row = int64_t(row0) + h;
-    uint16_t* dst = out + row * kDCkv + 16 * lane;
+    uint16_t* dst = out + row * kDCkv + 4 * t;
     if (n == 0) {                                   // empty context: o = 0, lse = -inf
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(0, 0, 0, 0);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(0, 0, 0, 0);
-        if (lane == 0) lse[row] = -INFINITY;
+        *reinterpret_cast<uint2*>(dst) = make_uint2(0, 0);
+        if (t == 0) lse[row] = -INFINITY;
         return;
     }
-    float m = -INFINITY;
-    for (int c = 0; c < n; c += 32)
-        if (c + lane < n) m = fmaxf(m, part_lse[int64_t(first + c + lane) * part_rows + h]);
+    float m = -INFINITY, wsum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c = 0; c < n; c += kMergeBatch) {
+        float l[kMergeBatch];
+        float4 v[kMergeBatch];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float acc[16];
-#pragma unroll
-    for (int d = 0; d < 16; ++d) acc[d] = 0.f;
-    float wsum = 0.f;
-    for (int c = 0; c < n; c += 32) {
-        // a partial whose tokens the row cannot see (extend) has lse = -inf and
-        // o = 0: weight 0
-        const float w = (c + lane < n) ? expf(part_lse[int64_t(first + c + lane) * part_rows + h] - m) : 0.f;
-        wsum += w;
-        const int cnt = min(32, n - c);
-        for (int i = 0; i < cnt; ++i) {
-            const float wi = __shfl_sync(0xffffffffu, w, i);
-            const float4* src =
-                reinterpret_cast<const float4*>(part_o + (int64_t(first + c + i) * part_rows + h) * kDCkv) + 4 * lane;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = src[q];
-                acc[4 * q] += wi * v.x;
-                acc[4 * q + 1] += wi * v.y;
-                acc[4 * q + 2] += wi * v.z;
-                acc[4 * q + 3] += wi * v.w;
-            }
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const bool ok = c + i < n;
+            const int64_t pr = int64_t(first + (ok ? c + i : 0)) * part_rows + h;
+            // a partial whose tokens the row cannot see (extend) has lse = -inf
+            // and o = 0: weight 0
+            l[i] = ok ? part_lse[pr] : -INFINITY;
+            v[i] = ok ? reinterpret_cast<const float4*>(part_o + pr * kDCkv)[t] : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        float mc = m;
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) mc = fmaxf(mc, l[i]);
+        const float r = m == -INFINITY ? 0.f : expf(m - mc);
+        acc.x *= r;
+        acc.y *= r;
+        acc.z *= r;
+        acc.w *= r;
+        wsum *= r;
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const float w = l[i] == -INFINITY ? 0.f : expf(l[i] - mc);
+            wsum += w;
+            acc.x += w * v[i].x;
+            acc.y += w * v[i].y;
+            acc.z += w * v[i].z;
+            acc.w += w * v[i].w;
+        }
+        m = mc;
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     const float inv = 1.f / wsum;
-    uint32_t pk[8];
-#pragma unroll
-    for (int d = 0; d < 8; ++d) pk[d] = pack_bf16x2(acc[2 * d] * inv, acc[2 * d + 1] * inv);
-    reinterpret_cast<uint4*>(dst)[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-    reinterpret_cast<uint4*>(dst)[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-    if (lane == 0) lse[row] = m + logf(wsum);
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    if (t == 0) lse[row] = m + logf(wsum);
 }
 
 std::mutex g_attr_mu;
@@ -558,7 +558,7 @@ mla_status_t run_plan(mla_plan_t plan, bool extend, const void* q, int64_t q_str
         // processed while the decode's last CTAs finish, and its blocks wait
         // on the device for the decode's partials
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(s.n_merge(), (s.part_rows + 3) / 4);
+        cfg.gridDim = dim3(s.n_merge(), s.part_rows);
         cfg.blockDim = dim3(128);
         cfg.stream = cs;
         cudaLaunchAttribute attr[1];
