@@ -933,8 +933,12 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
     }
 }
 
+// 152 registers at G = 16 (no spills): with 3 warps per SM sub-partition
+// that leaves room for one warp of the q split kernel beside the CTA, so the
+// programmatic launch places decode CTAs while the split still runs (at 160
+// registers they waited for the split to drain; measured on GB300).
 template <int G, bool E>
-__global__ void __launch_bounds__(kThreads, 1) mla_decode_tc_kernel(const DecodeParams p) {
+__global__ void __maxnreg__(G == 16 ? 152 : 168) mla_decode_tc_kernel(const DecodeParams p) {
     using S = Shape<G>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1022,6 +1026,12 @@ cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int d
             const cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<G, E>,
                                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
             if (e != cudaSuccess) return e;
+            // the split uses no shared memory; an SM configured for it with a
+            // small carveout could not take a decode CTA until it drained
+            const cudaError_t e2 = cudaFuncSetAttribute(mla_q_split_kernel<G>,
+                                                        cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                        cudaSharedmemCarveoutMaxShared);
+            if (e2 != cudaSuccess) return e2;
             g_attr[dev] |= bit;
         }
     }
