@@ -528,6 +528,7 @@ mla_status_t run_plan(mla_plan_t plan, bool extend, const void* q, int64_t q_str
     p.part_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + s.partial_lse_offset);
     p.cta_ptr = plan->dev_meta + plan->off_cta;
     p.segs = plan->dev_meta + plan->off_segs;
+    p.seg_pages = plan->dev_meta + plan->off_seg_pages;
     p.flags = device_flags_ptr();
     p.qimg = static_cast<uint8_t*>(workspace) + s.qimg_offset;
     p.batch = s.batch;

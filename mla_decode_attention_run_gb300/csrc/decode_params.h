@@ -25,6 +25,7 @@ struct DecodeParams {
     float* part_lse;            // [partials][H]
     const int32_t* cta_ptr;     // plan: segments of CTA c are [cta_ptr[c], cta_ptr[c+1])
     const int32_t* segs;        // plan: 4 ints per segment: request, t0, t1, partial (-1 final)
+    const int32_t* seg_pages;   // plan: per segment, kv_indptr of its request
     uint32_t* flags;            // library flag word
     uint8_t* qimg;              // tcgen05 path: per-request q images (workspace)
     int32_t batch;

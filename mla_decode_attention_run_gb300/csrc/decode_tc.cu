@@ -206,12 +206,25 @@ struct TileCursor {
     int32_t pg[2];                      // page entry, or kNoRow past the context
     int32_t t[2];                       // token index of each row
 
-    __device__ void init(const DecodeParams& p, int lo, int hi) {
+    __device__ void init(const DecodeParams& p, int lo, int hi, int lane) {
         si = lo;
         seg_hi = hi;
-        it = 0;
-        while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
-        if (si < seg_hi) pages = p.indices + p.indptr[sg.req];
+        seek(p, lane);
+    }
+    // Moves to the first segment from si on that has tiles and requests its
+    // first tile's page entries.  The plan carries each segment's page-table
+    // offset, so those loads go out with the segment record, before the
+    // context check (seq_lens) resolves; they stay inside the planned page
+    // table either way.
+    __device__ void seek(const DecodeParams& p, int lane) {
+        while (si < seg_hi) {
+            pages = p.indices + p.seg_pages[si];
+            sg = load_seg<E>(p, si);
+            it = 0;
+            prefetch(p, lane);
+            if (sg.ntiles > 0) break;
+            ++si;
+        }
     }
     __device__ bool valid() const { return si < seg_hi; }
     // issue the (independent) index loads of the current tile; nothing waits
@@ -234,12 +247,13 @@ struct TileCursor {
             slot[q] = ok ? static_cast<int32_t>(s) : -1;
         }
     }
-    __device__ void advance(const DecodeParams& p) {
+    // next tile, its page entries requested
+    __device__ void advance(const DecodeParams& p, int lane) {
         if (++it == sg.ntiles) {
-            it = 0;
             ++si;
-            while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
-            if (si < seg_hi) pages = p.indices + p.indptr[sg.req];
+            seek(p, lane);
+        } else {
+            prefetch(p, lane);
         }
     }
 };
@@ -278,8 +292,7 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     // one prefetch sweep per row when k_pe follows c_kv in the same row
     const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
     TileCursor<E> cur;
-    cur.init(p, seg_lo, seg_hi);
-    if (cur.valid()) cur.prefetch(p, lane);
+    cur.init(p, seg_lo, seg_hi, lane);
     // publishes every tile as soon as its ring entry is free (the ring bounds
     // how far ahead of the softmax warps the prefetches run)
     for (int n = 0; cur.valid(); ++n) {
@@ -287,8 +300,7 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
         const uint32_t u = static_cast<uint32_t>(n / kRing);
         int32_t sl[2];
         cur.rows(p, sl);
-        cur.advance(p);
-        if (cur.valid()) cur.prefetch(p, lane);       // the next tile's index loads fly meanwhile
+        cur.advance(p, lane);                         // the next tile's index loads fly meanwhile
         if (!mbar_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {

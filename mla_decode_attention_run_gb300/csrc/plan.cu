@@ -205,6 +205,8 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
         else if (seq[r] == 0) s.merge.insert(s.merge.end(), {r * H, 0, 0, H});
     }
     s.part_rows = H;
+    s.seg_pages.resize(s.n_segs());
+    for (int32_t i = 0; i < s.n_segs(); ++i) s.seg_pages[i] = indptr[s.segs[4 * i]];
     size_workspace(s, static_cast<int64_t>(B) * s.head_groups);
     return MLA_OK;
 }
@@ -296,6 +298,8 @@ mla_status_t build_extend_schedule(const int32_t* qo, const int32_t* indptr, con
             s.merge.insert(s.merge.end(), {s.blocks[4 * v + 1], first_partial[v], segs_per_block[v],
                                            s.blocks[4 * v + 2]});
     s.part_rows = static_cast<int32_t>(G);
+    s.seg_pages.resize(s.n_segs());
+    for (int32_t i = 0; i < s.n_segs(); ++i) s.seg_pages[i] = indptr[s.blocks[4 * s.segs[4 * i]]];
     size_workspace(s, nb);
     return MLA_OK;
 }
@@ -403,8 +407,8 @@ mla_status_t install(mla_plan_t* plan, Schedule&& s, size_t* workspace_bytes, vo
         return MLA_ERR_INVALID_ARG;       // a plan belongs to one device
     }
     p->device = dev;
-    const size_t need =
-        static_cast<size_t>(s.num_ctas + 1) + s.segs.size() + s.merge.size() + s.blocks.size();
+    const size_t need = static_cast<size_t>(s.num_ctas + 1) + s.segs.size() + s.merge.size() +
+                        s.blocks.size() + s.seg_pages.size();
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
     if (!p->upload_done &&
@@ -447,6 +451,7 @@ mla_status_t install(mla_plan_t* plan, Schedule&& s, size_t* workspace_bytes, vo
     p->off_segs = s.num_ctas + 1;
     p->off_merge = p->off_segs + s.segs.size();
     p->off_blocks = p->off_merge + s.merge.size();
+    p->off_seg_pages = p->off_blocks + s.blocks.size();
     std::memcpy(p->pinned + p->off_cta, s.cta_ptr.data(), (s.num_ctas + 1) * sizeof(int32_t));
     if (!s.segs.empty())
         std::memcpy(p->pinned + p->off_segs, s.segs.data(), s.segs.size() * sizeof(int32_t));
@@ -454,6 +459,8 @@ mla_status_t install(mla_plan_t* plan, Schedule&& s, size_t* workspace_bytes, vo
         std::memcpy(p->pinned + p->off_merge, s.merge.data(), s.merge.size() * sizeof(int32_t));
     if (!s.blocks.empty())
         std::memcpy(p->pinned + p->off_blocks, s.blocks.data(), s.blocks.size() * sizeof(int32_t));
+    if (!s.seg_pages.empty())
+        std::memcpy(p->pinned + p->off_seg_pages, s.seg_pages.data(), s.seg_pages.size() * sizeof(int32_t));
     if (cudaMemcpyAsync(p->dev_meta, p->pinned, need * sizeof(int32_t), cudaMemcpyHostToDevice,
                         cs) != cudaSuccess ||
         cudaEventRecord(p->upload_done, cs) != cudaSuccess) {

@@ -49,6 +49,8 @@ struct Schedule {
                                      // partial (-1 = final)
     std::vector<int32_t> merge;      // 4 per entry: first output row, first partial,
                                      // n partials, rows
+    std::vector<int32_t> seg_pages;  // per segment: its request's first page-table entry
+                                     // (kv_indptr[request]), so the kernel need not look it up
     int32_t part_rows = 0;           // rows per partial slot: H (decode), group_heads (extend)
     int32_t n_partials = 0;
     // extend: the query rows (new token x head, row = token * H + head) of
@@ -95,5 +97,5 @@ struct mla_plan {
     int32_t* pinned = nullptr;        // staging for the upload
     size_t pinned_cap = 0;
     cudaEvent_t upload_done = nullptr;
-    size_t off_cta = 0, off_segs = 0, off_merge = 0, off_blocks = 0;   // element offsets in dev_meta
+    size_t off_cta = 0, off_segs = 0, off_merge = 0, off_blocks = 0, off_seg_pages = 0;   // in dev_meta
 };
