@@ -106,6 +106,18 @@ MLA_DEVINLINE uint16_t bf16x2_to_e4m3x2_scaled(uint32_t word, float k_scale) {
     return two;
 }
 
+// Two f16 (low half = first) -> two E4M3 bytes (nearest even, saturating).
+MLA_DEVINLINE uint16_t f16x2_to_e4m3x2(uint32_t h) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;\n" : "=h"(r) : "r"(h));
+    return r;
+}
+MLA_DEVINLINE uint32_t sub_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
 MLA_DEVINLINE uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));

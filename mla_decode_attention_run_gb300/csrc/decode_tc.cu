@@ -746,33 +746,28 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
             mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
             fence_after_sync();
-            // lanes 0-15 hold the token's G heads: column h (q1 term) + G + h (q2)
-            float sum[G];
-#pragma unroll
-            for (int c = 0; c < S::kN / 16; c += 2) {     // two loads in flight per wait
-                uint32_t r[2][16];
-                tmem_ld16(w.tmem_lane + kColS + S::kN * slot + 16 * c, r[0]);
-                tmem_ld16(w.tmem_lane + kColS + S::kN * slot + 16 * c + 16, r[1]);
+            // the warp's 16 token rows sit in lanes 0-15 of its TMEM quadrant:
+            // threads 0-15 read heads 0 .. G/2 - 1 of their row, threads 16-31
+            // heads G/2 .. G - 1 of the same row (term 1 at column h, term 2 at
+            // column G + h)
+            float s[kHL];
+            {
+                uint32_t r1[kHL], r2[kHL];
+                if constexpr (kHL == 8) {
+                    tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot, r1);
+                    tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot + G, r2);
+                } else {
+                    tmem_ld_half16<kHL>(w.tmem_lane + kColS + S::kN * slot, r1);
+                    tmem_ld_half16<kHL>(w.tmem_lane + kColS + S::kN * slot + G, r2);
+                }
                 tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int h = (16 * (c + cc)) % G + t;
-                        sum[h] = 16 * (c + cc) < G ? __uint_as_float(r[cc][t]) : sum[h] + __uint_as_float(r[cc][t]);
-                    }
+                for (int j = 0; j < kHL; ++j)
+                    s[j] = valid ? (__uint_as_float(r1[j]) + __uint_as_float(r2[j])) * coef[w.hb + j] : -INFINITY;
             }
             fence_before_sync();
             mbar_arrive(&w.bars[S_FREE + slot]);
 
-            // the second half of the heads moves to lanes 16-31
-            float s[kHL];
-#pragma unroll
-            for (int j = 0; j < kHL; ++j) {
-                const float hi = __shfl_sync(0xffffffffu, sum[kHL + j], w.lane & 15);
-                const float raw = w.hb ? hi : sum[j];
-                s[j] = valid ? raw * coef[w.hb + j] : -INFINITY;
-            }
             if constexpr (E) {
                 const int tile_t0 = sg.t0 + it * kTT;
                 if (tile_t0 + kTT > mask_from) {    // token tile_t0 + srow is hidden from rows
@@ -834,12 +829,13 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                     const int j = 4 * e2 + 2 * hh;
                     const float x0 = m[j] == -INFINITY ? 0.f : fast_exp2(s[j] - m[j]) * kPScale;
                     const float x1 = m[j + 1] == -INFINITY ? 0.f : fast_exp2(s[j + 1] - m[j + 1]) * kPScale;
+                    // x = p1 + p2: p1 the nearest E4M3, p2 the nearest E4M3 to
+                    // the remainder, taken in f16 (x <= 256 keeps 11 bits there,
+                    // and f16(x) - p1 is exact); the denominator sums x itself
                     const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
-                    const float2 d1 = e4m3x2_to_float2(b1);
-                    const uint16_t b2 = f32x2_to_e4m3x2(x0 - d1.x, x1 - d1.y);
-                    const float2 d2 = e4m3x2_to_float2(b2);
-                    l[j] += d1.x + d2.x;
-                    l[j + 1] += d1.y + d2.y;
+                    const uint16_t b2 = f16x2_to_e4m3x2(sub_f16x2(pack_f16x2(x0, x1), e4m3x2_to_f16x2(b1)));
+                    l[j] += x0;
+                    l[j + 1] += x1;
                     w1 |= static_cast<uint32_t>(b1) << (16 * hh);
                     w2 |= static_cast<uint32_t>(b2) << (16 * hh);
                 }

@@ -107,6 +107,27 @@ MLA_DEVINLINE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// M = 64 accumulators keep a warp's 16 rows in lanes 0-15 of its lane
+// quadrant.  This load gives threads 0-15 those 16 lanes at columns
+// col .. col + N - 1 and threads 16-31 the same lanes at columns
+// col + kSplit .. (the 16x32bx2 shape), so both halves of the warp get data.
+template <int kSplit>
+MLA_DEVINLINE void tmem_ld_half8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr), "n"(kSplit));
+}
+template <int kSplit>
+MLA_DEVINLINE void tmem_ld_half16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr), "n"(kSplit));
+}
+
 MLA_DEVINLINE void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 // 32 lanes x 16 columns: thread t writes lane (base + t).

@@ -76,6 +76,7 @@ def _check(lens, q_lens, heads, ps=1, num_sms=152):
     ([40, 17, 33], [0, 17, 5], 4, 1),              # a request without new tokens
     ([700, 900], [8, 1], 128, 64),                 # many heads, paged
     ([64, 128], [64, 128], 16, 16),
+    ([0, 50, 0], [0, 7, 0], 16, 1),                # empty contexts beside an extend
 ])
 def test_extend_schedule_covers_rows_and_contexts(lens, q_lens, heads, ps):
     _check(lens, q_lens, heads, ps)

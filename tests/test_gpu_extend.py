@@ -124,3 +124,23 @@ def test_extend_full_size_sampled(name, requests):
                                            w.softmax_scale)
         check_attention(out[qo[b]:qo[b + 1]], lse[qo[b]:qo[b + 1]], o_ref, lse_ref,
                         f"{name} request {b}")
+
+
+def test_long_prefill_sampled_rows():
+    """A 1,024-token prefill (no cached prefix): 512 blocks of 32 rows, split
+    over the CTAs; sampled new tokens (first, tile edges, last) against the
+    oracle's decode over each token's visible prefix."""
+    L = 1024
+    w = W.make_extend_workload("single", L, batch=1, lens=[L], num_slots=4096, std=0.5)
+    pool = oracle_pool(w)
+    dpool = torch.from_numpy(pool).cuda()
+    out, lse, plan = gpu_extend(w, dpool[:, :512], dpool[:, 512:])
+    assert M.mla_get_last_error() == 0
+    assert M.mla_decode_plan_info(plan)["num_ctas"] > 100
+    for i in (0, 1, 63, 64, 65, 127, 500, 1022, 1023):
+        visible = i + 1
+        o_ref, lse_ref = oracle.decode_fp8(w.q_bf16[i:i + 1], pool[:, :512], pool[:, 512:],
+                                           np.array([0, visible], np.int32),
+                                           w.kv_indices[:visible], np.array([visible], np.int32),
+                                           1, w.k_scale, w.softmax_scale)
+        check_attention(out[i:i + 1], lse[i:i + 1], o_ref, lse_ref, f"prefill token {i}")
