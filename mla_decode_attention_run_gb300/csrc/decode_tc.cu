@@ -34,9 +34,15 @@
 // O accumulates in TMEM across a segment's tiles; when m does move, the
 // softmax warps rescale it in place before the next PV may add to it.
 //
-// A CTA serves 16 heads of its token range; more heads run as more CTAs
-// (grid.y = head group).  The groups of a token range start together, so
-// their repeated reads of the same rows mostly hit L2.
+// A CTA serves G = 16 or 32 heads of its token range (32 when H is a multiple
+// of 32); more heads run as more CTAs (grid.y = head group).  The groups of a
+// token range start together, so their repeated reads of the same rows
+// mostly hit L2.
+//
+// Extend (several new tokens per request, causal) is the same kernel built
+// with E = true: a CTA then serves a block of G query rows (token x head) of
+// one request, each with its own causal limit; the softmax hides the tokens
+// at or past a row's limit on the tiles that reach them.
 //
 // Warp roles (one CTA per SM, persistent over its token range):
 //   warp 11    publishes tiles ahead of the stage fills: resolves each row's
@@ -52,13 +58,15 @@
 //   warp 4     one thread issues the QK^T MMAs, tile after tile;
 //   warp 10    one thread issues the PV MMAs, so that PV of one tile never
 //              waits behind QK^T of the next;
-//   warp 5     fetches each segment's [q1;q2] image and per-head score
-//              multipliers, written by the q split kernel that precedes this
-//              one (double-buffered);
-//   warps 6-9  online softmax of a token's 16 heads and the E4M3 split of P
+//   warp 5     fetches each segment's [q1;q2] image, per-row score
+//              multipliers and causal limits, written by the q split kernel
+//              that precedes this one (double-buffered for G = 16);
+//   warps 6-9  online softmax of a token's G heads and the E4M3 split of P
 //              (an M = 64 accumulator puts a tile's rows in lanes 0-15 of
-//              each warp's TMEM lane quadrant), rescaling O when the maximum
-//              moves, and the epilogue (all lanes: lane = output channel).
+//              each warp's TMEM lane quadrant; threads 0-15 take the first
+//              half of the heads, 16-31 the second), rescaling O when the
+//              maximum moves, and the epilogue (all lanes: lane = output
+//              channel).
 // Every mbarrier wait is bounded; on a timeout the CTA sets
 // MLA_FLAG_WAIT_TIMEOUT, drains its MMAs and copies, frees TMEM and exits.
 #include <mutex>
