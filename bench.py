@@ -378,9 +378,18 @@ def run_ours(args, rank, world, local):
     # time on two copy streams, so that each chunk's copies overlap the
     # neighbouring chunks' store + decode (every byte still crosses within the
     # timed step).
-    n_chunks = 6
-    bounds = [L * c // n_chunks for c in range(n_chunks + 1)]
+    # small chunks at both ends (the first upload and the last download are
+    # not hidden), large ones in the middle
+    ramp = [2, 4, 8]
+    sizes = ramp + [max(1, (L - 2 * sum(ramp)) // 3)] * 3 + ramp[::-1]
+    if sum(sizes) > L or L < 2 * sum(ramp) + 3:
+        sizes = [L]
+    sizes[len(sizes) // 2] += L - sum(sizes)
+    bounds = [0]
+    for z in sizes:
+        bounds.append(bounds[-1] + z)
     spans = list(zip(bounds[:-1], bounds[1:]))
+    n_chunks = len(spans)
     g_chunks = [capture(lambda s, a=a, b=b: [(store(l, s), decode(l, s)) for l in range(a, b)])
                 for a, b in spans]
     up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
@@ -432,8 +441,8 @@ def run_ours(args, rank, world, local):
                      "unit": "us/call",
                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                      "per": "layer-call incl. store and host copies",
-                     "overlap": f"inputs up and outputs down per chunk of {L // n_chunks}-{-(-L // n_chunks)} "
-                                "layers on two copy streams, overlapping compute"}
+                     "overlap": f"inputs up and outputs down per chunk of layers {sizes} on two copy "
+                                "streams, overlapping compute"}
 
     # ---- the two baselines the pages describe, per decode step
     if not args.no_baselines:
