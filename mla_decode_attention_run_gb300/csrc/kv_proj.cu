@@ -22,10 +22,17 @@
 // once per stage buffer while the first loads are in flight.  No workspace,
 // no second launch.
 //
+// A batch of at most 64 tokens runs M = 64 MMAs: 8 KB token tiles and 4
+// stages keep a CTA at 86 KB of shared memory, two per SM.  The kernel is
+// launched as a programmatic dependent of the kernel before it: the first
+// weight chunks are requested before griddepcontrol.wait, the hidden states
+// after it.
+//
 // Warps: 0-1 load, lane 0 of warp 2 issues the MMAs, warps 2-5 (one per TMEM
 // lane quadrant) read the accumulator out.  Waits are bounded; after a
 // timeout the CTA still reaches the cluster barrier, so no CTA of its
 // cluster waits forever.
+#include <array>
 #include <cmath>
 #include <mutex>
 #include <vector>
@@ -43,18 +50,19 @@ constexpr int kPK = 64;                      // K elements per stage: one 128-by
 constexpr int kPLoadWarps = 2;
 constexpr int kPThreads = 192;
 constexpr int kPMaxSplit = 16;               // cluster size (8 is portable; 16 where allowed)
-constexpr int kATile = kPM * 128;            // 16 KB
-
-// Shared-memory map for N latent channels per tile.
-template <int N>
+// Shared-memory map for M token rows (MMA M: 128, or 64 for a batch of at
+// most 64 tokens, whose smaller tiles let two CTAs share an SM) and N latent
+// channels per tile.
+template <int N, int M>
 struct ProjShape {
+    static constexpr int kATile = M * 128;
     static constexpr int kBTile = N * 128;
     static constexpr int kStage = kATile + kBTile;
-    static constexpr int kStages = N == 32 ? 8 : 6;
+    static constexpr int kStages = M == 64 ? 4 : 6;
     static constexpr int kRedStride = N + 4;            // floats per partial-tile row (spreads banks)
     static constexpr int kOffRed = kStages * kStage;
-    // partial rows received from the cluster: split x ceil(128 / split) rows
-    static constexpr int kRedRows = kPM + kPMaxSplit;
+    // partial rows received from the cluster: split x ceil(M / split) rows
+    static constexpr int kRedRows = M + kPMaxSplit;
     static constexpr int kOffBar = kOffRed + kRedRows * kRedStride * 4;
     static constexpr int kNumBars = 2 * kStages + 2;    // full[], empty[], done, zero
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -62,7 +70,7 @@ struct ProjShape {
     static constexpr uint32_t kTmemCols = N;
     static_assert(kSmem <= 227 * 1024, "shared memory budget");
     static_assert(kDCkv % N == 0 && kDKpe % N == 0, "a channel tile lies in c_kv or in k_pe");
-    static_assert(kStage % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(kStage % 1024 == 0 && kATile % 1024 == 0, "swizzle atoms need 1 KB alignment");
 };
 static_assert(kDQk % 64 == 0 && kDCkv % 64 == 0, "a channel tile lies in c_kv or in k_pe");
 
@@ -84,9 +92,9 @@ struct ProjParams {
     uint32_t* flags;
 };
 
-template <int N>
+template <int N, int M>
 __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjParams p) {
-    using S = ProjShape<N>;
+    using S = ProjShape<N, M>;
     constexpr int kStages = S::kStages;
     constexpr int FULL = 0, EMPTY = kStages, DONE = 2 * kStages, ZERO = 2 * kStages + 1;
     extern __shared__ uint8_t smem_raw[];
@@ -99,8 +107,8 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
     const int split = gridDim.x;                  // = the cluster size along K
     const int rank = static_cast<int>(cluster_ctarank());
     const int n0 = blockIdx.y * N;
-    const int64_t m0 = int64_t(blockIdx.z) * kPM;
-    const int rows = p.n - m0 < kPM ? static_cast<int>(p.n - m0) : kPM;   // token rows of this tile
+    const int64_t m0 = int64_t(blockIdx.z) * M;
+    const int rows = p.n - m0 < M ? static_cast<int>(p.n - m0) : M;   // token rows of this tile
     const int c_lo = p.kchunks * rank / split, c_hi = p.kchunks * (rank + 1) / split;
     const int nch = c_hi - c_lo;                  // >= 1: the host keeps split <= kchunks
 
@@ -121,30 +129,45 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kPLoadWarps) {
-        // stage = A: 128 token rows x 128 B (rows past the batch stay zero),
-        // B: N weight rows x 128 B; 16-byte chunk c of row r at c ^ (r & 7)
-        for (int i = 0; i < nch; ++i) {
-            const int s = i % kStages;
-            const uint32_t u = static_cast<uint32_t>(i / kStages);
-            if (!mbar_wait(&bars[EMPTY + s], (u & 1) ^ 1, abort, p.flags)) break;
-            uint8_t* a = base + s * S::kStage;
-            uint8_t* b = a + kATile;
+        // stage = A: M token rows x 128 B (rows past the batch stay zero),
+        // B: N weight rows x 128 B; 16-byte chunk c of row r at c ^ (r & 7).
+        // The weights do not depend on the kernel before this one (the launch
+        // is its programmatic dependent): the first ring's weight chunks go
+        // out at once, the hidden states after griddepcontrol.wait.
+        const int pre = nch < kStages ? nch : kStages;
+        auto load_b = [&](int i) {
+            uint8_t* b = base + (i % kStages) * S::kStage + S::kATile;
             const int64_t k0 = int64_t(c_lo + i) * kPK;
-            for (int q = tid; q < rows * 8; q += 32 * kPLoadWarps) {
-                const int r = q >> 3, c = q & 7;
-                cp_async16(a + r * 128 + ((c ^ (r & 7)) << 4), p.x + (m0 + r) * p.x_stride + k0 + c * 8, 16u);
-            }
 #pragma unroll
             for (int j = 0; j < N * 8 / (32 * kPLoadWarps); ++j) {
                 const int q = tid + 32 * kPLoadWarps * j, r = q >> 3, c = q & 7;
                 cp_async16(b + r * 128 + ((c ^ (r & 7)) << 4), p.w + int64_t(n0 + r) * p.w_stride + k0 + c * 8, 16u);
             }
+        };
+        auto load_a = [&](int i) {
+            uint8_t* a = base + (i % kStages) * S::kStage;
+            const int64_t k0 = int64_t(c_lo + i) * kPK;
+            for (int q = tid; q < rows * 8; q += 32 * kPLoadWarps) {
+                const int r = q >> 3, c = q & 7;
+                cp_async16(a + r * 128 + ((c ^ (r & 7)) << 4), p.x + (m0 + r) * p.x_stride + k0 + c * 8, 16u);
+            }
+        };
+        for (int i = 0; i < pre; ++i) load_b(i);        // stages start empty: no wait
+        griddep_wait();
+        for (int i = 0; i < nch; ++i) {
+            const int s = i % kStages;
+            const uint32_t u = static_cast<uint32_t>(i / kStages);
+            if (!mbar_wait(&bars[EMPTY + s], (u & 1) ^ 1, abort, p.flags)) break;
+            if (i >= pre) load_b(i);
+            load_a(i);
+            // arrives once this thread's copies so far (this stage's among
+            // them) have landed
             mbar_arrive_cp_async(&bars[FULL + s]);
         }
         cp_async_wait<0>();
     } else if (warp == 2) {
         if (lane == 0) {
-        const uint32_t idesc = idesc_bf16_f32(kPM, N);
+        const uint32_t idesc = idesc_bf16_f32(M, N);
         // the zeroed rows must be in place before the first MMA reads them
         const bool zeroed = mbar_wait(&bars[ZERO], 0, abort, p.flags);
         for (int i = 0; zeroed && i < nch; ++i) {
@@ -155,7 +178,7 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
             fence_proxy_async_smem();
             const uint32_t sa = smem_u32(base + s * S::kStage);
             const uint64_t ad = smem_desc(sa, 16, 1024, kSwizzle128B);
-            const uint64_t bd = smem_desc(sa + kATile, 16, 1024, kSwizzle128B);
+            const uint64_t bd = smem_desc(sa + S::kATile, 16, 1024, kSwizzle128B);
 #pragma unroll
             for (int ks = 0; ks < kPK / 16; ++ks)       // K = 16 per MMA: 32 bytes along the row
                 mma_bf16(tmem, ad + static_cast<uint64_t>(ks * 2), bd + static_cast<uint64_t>(ks * 2), idesc,
@@ -166,7 +189,7 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
         }
     } else {
         // warps 3-5: token rows past the batch, zero in every stage, once
-        for (int q = rows * 8 + (tid - 96); q < kPM * 8; q += 96) {
+        for (int q = rows * 8 + (tid - 96); q < M * 8; q += 96) {
             const int r = q >> 3, c = q & 7;
 #pragma unroll 1
             for (int s = 0; s < kStages; ++s)
@@ -178,22 +201,24 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
     }
     __syncwarp();
 
-    // this CTA's partial of tile row r (= TMEM lane) goes to CTA r mod S of
-    // the cluster, partial slot [rank][r / S]
-    const int rpo = (kPM + split - 1) / split;            // rows per owning CTA
+    // this CTA's partial of tile row r goes to CTA r mod S of the cluster,
+    // partial slot [rank][r / S].  M = 128: row r in TMEM lane r; M = 64:
+    // rows 16 q .. 16 q + 15 in lanes 0-15 of lane quadrant q
+    const int rpo = (M + split - 1) / split;              // rows per owning CTA
     if (warp >= 2) {
         const int q = warp & 3;
-        const int row = q * 32 + lane;
+        const int row = M == 128 ? q * 32 + lane : (lane < 16 ? q * 16 + lane : M);
         const bool ok = mbar_wait(&bars[DONE], 0, abort, p.flags);
         fence_after_sync();
-        const uint32_t dst = cluster_map(smem_u32(red + (rank * rpo + row / split) * S::kRedStride),
-                                         static_cast<uint32_t>(row % split));
+        const int prow = row < rows ? row : 0;            // address only used when row < rows
+        const uint32_t dst = cluster_map(smem_u32(red + (rank * rpo + prow / split) * S::kRedStride),
+                                         static_cast<uint32_t>(prow % split));
 #pragma unroll
         for (int c = 0; c < N; c += 16) {
             uint32_t r[16];
             tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c, r);
             tmem_wait_ld();
-            if (row < rows) {
+            if (row < rows) {                             // (a row of M never is)
 #pragma unroll
                 for (int e = 0; e < 16; e += 4)
                     st_cluster_f4(dst + 4 * (c + e),
@@ -206,6 +231,10 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
     fence_before_sync();
     __syncthreads();
     cluster_sync();                                       // every partial row has arrived
+    // the next kernel may be launched (a programmatic dependent still waits
+    // for this grid to complete before it reads what this grid wrote);
+    // signalling here rather than at the start measured faster
+    if (tid == 0) griddep_launch_dependents();
 
     // rows rank, rank + S, ...: sum the S partials (in rank order), round to
     // BF16, quantize, store
@@ -245,24 +274,24 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
 
 std::mutex g_proj_mu;
 std::vector<char> g_proj_attr;      // per device: bit (N / 32 - 1): attributes set
-std::vector<int> g_proj_max_split;  // per device: widest cluster the device accepts
-std::vector<std::vector<int>> g_proj_fit;   // per device, per split: clusters that fit at once
+std::vector<std::array<int, 2>> g_proj_max_split;  // per device and M: widest cluster accepted
+std::vector<std::vector<int>> g_proj_fit;   // per device, per (M, split): clusters that fit at once
 
-template <int N>
+template <int N, int M>
 mla_status_t launch_proj(const ProjParams& p, int64_t m_tiles, int dev, cudaStream_t stream) {
-    using S = ProjShape<N>;
+    using S = ProjShape<N, M>;
     {
         std::lock_guard<std::mutex> lk(g_proj_mu);
         if ((int)g_proj_attr.size() <= dev) g_proj_attr.resize(dev + 1, 0);
-        const char bit = static_cast<char>(1 << (N / 32 - 1));
+        const char bit = static_cast<char>(1 << (M / 64 - 1));
         if (!(g_proj_attr[dev] & bit)) {
-            if (cudaFuncSetAttribute(kv_proj_store_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(kv_proj_store_kernel<N, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      S::kSmem) != cudaSuccess)
                 return MLA_ERR_CUDA;
-            if ((int)g_proj_max_split.size() <= dev) g_proj_max_split.resize(dev + 1, 8);
+            if ((int)g_proj_max_split.size() <= dev) g_proj_max_split.resize(dev + 1);
             // clusters of 16 are not portable: use them where the device allows
-            g_proj_max_split[dev] =
-                cudaFuncSetAttribute(kv_proj_store_kernel<N>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            g_proj_max_split[dev][M / 64 - 1] =
+                cudaFuncSetAttribute(kv_proj_store_kernel<N, M>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                         cudaSuccess
                     ? kPMaxSplit
                     : 8;
@@ -279,17 +308,22 @@ mla_status_t launch_proj(const ProjParams& p, int64_t m_tiles, int dev, cudaStre
     cfg.blockDim = dim3(kPThreads);
     cfg.dynamicSmemBytes = S::kSmem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // a programmatic dependent of the kernel before it: CTAs may start (and
+    // stream weights) while that kernel finishes; they wait for it on the
+    // device before reading the hidden states or writing the pool
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int split = 1;
     int max_split = 8;
     {
         std::lock_guard<std::mutex> lk(g_proj_mu);
-        max_split = g_proj_max_split[dev];
+        max_split = g_proj_max_split[dev][M / 64 - 1];
     }
     for (int s = max_split < p.kchunks ? max_split : p.kchunks; s > 1; --s) {
         if (tiles * s > device_sm_count()) continue;
@@ -299,15 +333,15 @@ mla_status_t launch_proj(const ProjParams& p, int64_t m_tiles, int dev, cudaStre
         {
             std::lock_guard<std::mutex> lk(g_proj_mu);
             if ((int)g_proj_fit.size() <= dev) g_proj_fit.resize(dev + 1);
-            if (g_proj_fit[dev].empty()) g_proj_fit[dev].assign(kPMaxSplit + 1, -1);
-            fit = g_proj_fit[dev][s];
-            if (fit < 0) {
-                if (cudaOccupancyMaxActiveClusters(&fit, kv_proj_store_kernel<N>, &cfg) != cudaSuccess) {
+            if (g_proj_fit[dev].empty()) g_proj_fit[dev].assign(2 * (kPMaxSplit + 1), -1);
+            int& slot = g_proj_fit[dev][(M / 64 - 1) * (kPMaxSplit + 1) + s];
+            if (slot < 0) {
+                if (cudaOccupancyMaxActiveClusters(&slot, kv_proj_store_kernel<N, M>, &cfg) != cudaSuccess) {
                     cudaGetLastError();
-                    fit = 0;
+                    slot = 0;
                 }
-                g_proj_fit[dev][s] = fit;
             }
+            fit = slot;
         }
         if (fit >= tiles) {
             split = s;
@@ -316,7 +350,8 @@ mla_status_t launch_proj(const ProjParams& p, int64_t m_tiles, int dev, cudaStre
     }
     cfg.gridDim = dim3(static_cast<unsigned>(split), kDQk / N, static_cast<unsigned>(m_tiles));
     attr[0].val.clusterDim.x = static_cast<unsigned>(split);
-    return cudaLaunchKernelEx(&cfg, kv_proj_store_kernel<N>, p) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kv_proj_store_kernel<N, M>, p) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -342,6 +377,7 @@ extern "C" mla_status_t kv_proj_store_fp8(const void* x, int64_t x_row_stride, c
         return MLA_ERR_UNSUPPORTED;
     const int64_t m_tiles = (n + kPM - 1) / kPM;
     if (m_tiles > 65535) return MLA_ERR_UNSUPPORTED;
+    const bool small = n <= 64;         // one 64-row token tile
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
     ProjParams p;
@@ -360,5 +396,6 @@ extern "C" mla_status_t kv_proj_store_fp8(const void* x, int64_t x_row_stride, c
     p.num_slots = num_pool_slots;
     p.latent = static_cast<uint16_t*>(latent_out);
     p.flags = device_flags_ptr();
-    return launch_proj<64>(p, m_tiles, dev, static_cast<cudaStream_t>(stream));
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    return small ? launch_proj<64, 64>(p, 1, dev, cs) : launch_proj<64, 128>(p, m_tiles, dev, cs);
 }
