@@ -45,11 +45,12 @@ namespace {
 
 using namespace tc;
 
-constexpr int kPM = 128;                     // token rows per tile (MMA M)
+constexpr int kPM = 128;                     // token rows per tile beyond 64 tokens (MMA M)
 constexpr int kPK = 64;                      // K elements per stage: one 128-byte row
 constexpr int kPLoadWarps = 2;
 constexpr int kPThreads = 192;
 constexpr int kPMaxSplit = 16;               // cluster size (8 is portable; 16 where allowed)
+
 // Shared-memory map for M token rows (MMA M: 128, or 64 for a batch of at
 // most 64 tokens, whose smaller tiles let two CTAs share an SM) and N latent
 // channels per tile.
