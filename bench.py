@@ -467,6 +467,8 @@ def run_ours(args, rank, world, local):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_from_device(pools[0], q[0], indptr, idx, lens,
                                                           k_scales[0])
+        if not args.no_configs:
+            result["cpu_oracle_configs"] = oracle_timings()
     del g_step, g_decode
     M.mla_decode_plan_destroy(plan)
     return result
@@ -788,6 +790,83 @@ def oracle_call(pool_np, q_bits, indptr, idx, lens, k_scale, nthreads=0):
     oracle.decode_fp8(q_bits, pool_np[:, :512], pool_np[:, 512:], indptr, idx, lens, PAGE,
                       k_scale, W.SOFTMAX_SCALE, nthreads=nthreads)
     return time.perf_counter() - t0
+
+
+def oracle_timings():
+    """The oracle beside each measured configuration, on this host's cores
+    (random pool bytes: timing does not depend on the values).  Small cases
+    single-threaded and on all cores; the 128-head call on one of its 128
+    requests, the 4-token extend on 4 of its 40 requests, both scaled
+    linearly by the work (labelled extrapolated); the projection store of
+    one layer in full."""
+    import oracle
+    rng = np.random.default_rng(3)
+    # taken before any call: a call with nthreads = 1 sets OpenMP's default
+    cores = oracle.max_threads()
+    res = {"cores": cores}
+
+    def timed_call(fn):
+        t0 = time.perf_counter()
+        fn()
+        return (time.perf_counter() - t0) * 1e6
+
+    def decode_case(name, requests=None, threads=(1, None)):
+        w = W.make_workload(name, latent_requests=[])
+        B = w.batch
+        keep = list(range(B)) if requests is None else requests
+        lens = w.seq_lens[keep]
+        ps = w.page_size
+        pages = [w.kv_indices[w.kv_indptr[b]:w.kv_indptr[b + 1]] for b in keep]
+        indptr = np.zeros(len(keep) + 1, np.int32)
+        indptr[1:] = np.cumsum([len(x) for x in pages])
+        idx = np.concatenate(pages).astype(np.int32)
+        pool = W.random_fill_bytes(rng, (w.num_slots, W.D_ALL))
+        q = w.q_bf16[keep]
+        out = {}
+        for t in threads:
+            nt = cores if t is None else t
+            us = timed_call(lambda: oracle.decode_fp8(q, pool[:, :512], pool[:, 512:], indptr, idx,
+                                                      lens, ps, w.k_scale, W.SOFTMAX_SCALE,
+                                                      nthreads=nt))
+            scale = float(w.seq_lens.sum()) / float(lens.sum())
+            out["us_per_call_" + ("1_thread" if t == 1 else "all_cores")] = round(us * scale, 1)
+        if requests is not None:
+            out["extrapolated"] = f"timed on {len(keep)} of {B} requests, scaled by tokens"
+        return out
+
+    res["tiny"] = decode_case("tiny")
+    res["single"] = decode_case("single")
+    res["concurrency"] = decode_case("concurrency", threads=(None,))
+    res["large_head"] = decode_case("large_head", requests=[0], threads=(None,))
+
+    w = W.make_extend_workload("spec_decode", latent_requests=[])
+    keep = [0, 1, 2, 3]
+    qo = w.extra["qo_indptr"]
+    sub_qo = np.zeros(len(keep) + 1, np.int32)
+    sub_qo[1:] = np.cumsum([qo[b + 1] - qo[b] for b in keep])
+    pages = [w.kv_indices[w.kv_indptr[b]:w.kv_indptr[b + 1]] for b in keep]
+    sub_ip = np.zeros(len(keep) + 1, np.int32)
+    sub_ip[1:] = np.cumsum([len(x) for x in pages])
+    sub_q = np.concatenate([w.q_bf16[qo[b]:qo[b + 1]] for b in keep])
+    pool = W.random_fill_bytes(rng, (w.num_slots, W.D_ALL))
+    us = timed_call(lambda: oracle.extend_fp8(sub_q, pool[:, :512], pool[:, 512:], sub_qo, sub_ip,
+                                              np.concatenate(pages).astype(np.int32),
+                                              w.seq_lens[keep], 1, w.k_scale, W.SOFTMAX_SCALE,
+                                              nthreads=cores))
+    ql = np.diff(qo)
+    scale = A.extend_visible_tokens(w.seq_lens, ql) / A.extend_visible_tokens(w.seq_lens[keep], ql[keep])
+    res["spec_decode"] = {"us_per_call_all_cores": round(us * scale, 1),
+                          "extrapolated": f"timed on {len(keep)} of {w.batch} requests, scaled by "
+                                          "visible tokens"}
+
+    n, d = 40, PROJ_D_MODEL
+    x = rng.integers(0, 1 << 16, size=(n, d), dtype=np.uint16) & 0xBFFF   # finite BF16 bit patterns
+    wts = rng.integers(0, 1 << 16, size=(W.D_ALL, d), dtype=np.uint16) & 0xBFFF
+    slots = rng.permutation(4096)[:n].astype(np.int64)
+    ppool = np.zeros((4096, W.D_ALL), np.uint8)
+    us = timed_call(lambda: oracle.kv_proj_fp8(x, wts, slots, 0.01, ppool[:, :512], ppool[:, 512:]))
+    res["kv_proj"] = {"us_per_layer_all_cores": round(us, 1)}
+    return res
 
 
 def cpu_baseline_from_device(pool_d, q_d, indptr, idx, lens, k_scale):
