@@ -88,8 +88,7 @@ constexpr int kTT = 64;
 constexpr int kM = 64;
 constexpr int kStages = 4;
 constexpr int kFillWarps = 4;
-constexpr int kWarpMma = 4, kWarpQ = 5, kWarpWg = 6, kWarpPv = 10, kWarpSched = 11;
-constexpr int kThreads = 384;
+constexpr int kWarpMma = 4, kWarpQ = 5;      // the other roles depend on G (Shape<G>)
 constexpr int kBlk = kTT * 128;             // 64 rows x 128 B, 128-byte swizzle (128 c_kv channels)
 constexpr int kRope = kTT * 64;             // 64 rows x 64 B, 64-byte swizzle (the 64 k_pe channels)
 constexpr int kStage = 4 * kBlk + kRope;    // 36 KB per tile
@@ -116,7 +115,13 @@ struct Shape {
     static constexpr int kQBufs = G == 16 ? 2 : 1;    // q buffers in shared memory
     static constexpr int kOBufs = G == 16 ? 2 : 1;    // O accumulators in TMEM
     static constexpr int kPBytes = (kN / 16) * kPUnit;    // [P1;P2]^T of one tile
-    static constexpr int kHL = G / 2;                 // heads per softmax lane
+    // softmax: one warpgroup per 16 heads, 8 heads per lane (threads 0-15 the
+    // first 8 of a token row, 16-31 the other 8)
+    static constexpr int kWgs = G / 16;
+    static constexpr int kThreads = 384 + 128 * (kWgs - 1);
+    static constexpr int kWarpWg = G == 16 ? 6 : 8;   // first softmax warp
+    static constexpr int kWarpPv = G == 16 ? 10 : 6;
+    static constexpr int kWarpSched = G == 16 ? 11 : 7;
     static constexpr uint32_t kColO = 2 * kN;         // TMEM: S[0], S[1], then O[b] + 4 kN b
     static constexpr int kImage = kQBytes + G * 8;    // q image + score multipliers + causal limits
     static_assert(kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
@@ -136,8 +141,8 @@ constexpr int kOffBar = kOffRing + kRing * kTT * 4;
 constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x G
 constexpr int kOffLsum = kOffRed + 2 * 4 * kMaxG * 4;   // softmax denominators: 4 warps x G
 constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // per q buffer: G multipliers, G limits
-constexpr int kOffFlag = kOffCoef + 2 * 16 * 8;         // rescale votes: 2 x 4 warps
-constexpr int kOffMisc = kOffFlag + 32;     // TMEM base, abort flag
+constexpr int kOffFlag = kOffCoef + 2 * 16 * 8;         // rescale votes: per warpgroup 2 x 4 warps
+constexpr int kOffMisc = kOffFlag + 64;     // TMEM base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 static_assert(Shape<16>::kQBufs * 16 * 8 <= 2 * 16 * 8 && Shape<32>::kQBufs * 32 * 8 <= 2 * 16 * 8,
               "multiplier and limit space");
@@ -146,8 +151,12 @@ static_assert(Shape<16>::kImage == kTcQImageBytes && Shape<32>::kImage == 2 * kT
 static_assert(kBlk % 1024 == 0 && kStage % 1024 == 0, "swizzle atoms need 1 KB alignment");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kTT == kM && kTcTileTokens % kTT == 0, "a tile fills the MMA's M; segments start on tiles");
-static_assert(kWarpPv == kWarpWg + 4 && kWarpSched == kWarpPv + 1 && kThreads == 32 * (kWarpSched + 1),
-              "warp roles");
+static_assert(Shape<16>::kWarpPv == Shape<16>::kWarpWg + 4 && Shape<16>::kWarpSched == Shape<16>::kWarpPv + 1 &&
+                  Shape<16>::kThreads == 32 * (Shape<16>::kWarpSched + 1),
+              "warp roles, 16 heads");
+static_assert(Shape<32>::kWarpPv == kWarpQ + 1 && Shape<32>::kWarpSched == Shape<32>::kWarpPv + 1 &&
+                  Shape<32>::kWarpWg == 8 && Shape<32>::kThreads == 32 * (Shape<32>::kWarpWg + 8),
+              "warp roles, 32 heads: warpgroups fill | issuers | softmax | softmax");
 
 enum : int {
     KV_FULL = 0, KV_EMPTY = kStages, S_FULL = 2 * kStages, S_FREE = S_FULL + 2, P_FULL = S_FREE + 2,
@@ -156,7 +165,6 @@ enum : int {
     NUM_BARS = SL_EMPTY + kRing
 };
 static_assert(NUM_BARS * 8 <= 512, "barrier space");
-static_assert(SL_FULL == 23, "barrier count table below assumes four stages");
 
 // b: the request, or (extend) the query block; req: the request whose pages
 // and context the segment reads
@@ -192,7 +200,12 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
     return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-__device__ __forceinline__ void wg_bar() { asm volatile("bar.sync 1, 128;\n" ::: "memory"); }
+// named barrier of softmax warpgroup g (ids 1, 2; 0 is __syncthreads),
+// immediate ids so that the kernel reserves only those
+__device__ __forceinline__ void wg_bar(int g) {
+    if (g == 0) asm volatile("bar.sync 1, 128;\n" ::: "memory");
+    else asm volatile("bar.sync 2, 128;\n" ::: "memory");
+}
 
 // ------------------------------------------------------------ producer warps
 //
@@ -642,33 +655,31 @@ struct WgCtx {
     uint32_t* flags;
     int row;                // TMEM lane of O = channel within a 128-channel block
     int srow;               // token of S (M = 64: lanes 0-15 of each lane quadrant)
-    int hb;                 // heads hb .. hb + G/2 - 1 of token srow are this lane's: lanes
-                            // 0-15 take the first half of the heads, 16-31 the second
-    int wq, lane;           // softmax warp 0..3, lane
+    int h0;                 // this warpgroup's heads: h0 .. h0 + 15
+    int hb;                 // heads hb .. hb + 7 of token srow are this lane's: lanes 0-15
+                            // take h0 .. h0 + 7, 16-31 h0 + 8 .. h0 + 15
+    int wg, wq, lane;       // softmax warpgroup, warp within it 0..3, lane
 };
 
-// O (one segment's accumulator) *= alpha per head, in TMEM.  Each
-// 128-channel block holds kN columns: head h's two P terms in columns h and
-// G + h.
+// O (one segment's accumulator) *= alpha per head, in TMEM, for the
+// warpgroup's 16 heads.  Each 128-channel block holds kN columns: head h's two
+// P terms in columns h and G + h.
 template <int G>
-__device__ __forceinline__ void rescale_o(const WgCtx& w, uint32_t ocol, const float (&alpha)[G]) {
+__device__ __forceinline__ void rescale_o(const WgCtx& w, uint32_t ocol, const float (&alpha)[16]) {
     using S = Shape<G>;
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) {
+        uint32_t r[2][16];
+        tmem_ld16(w.tmem_lane + ocol + S::kN * mb + w.h0, r[0]);
+        tmem_ld16(w.tmem_lane + ocol + S::kN * mb + G + w.h0, r[1]);
+        tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < S::kN / 16; c += 2) {         // two loads in flight per wait
-            uint32_t r[2][16];
-            tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c, r[0]);
-            tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c + 16, r[1]);
-            tmem_wait_ld();
+        for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    r[cc][i] = __float_as_uint(__uint_as_float(r[cc][i]) * alpha[(16 * (c + cc)) % G + i]);
-                tmem_st16(w.tmem_lane + ocol + S::kN * mb + 16 * (c + cc), r[cc]);
-            }
+            for (int i = 0; i < 16; ++i) r[cc][i] = __float_as_uint(__uint_as_float(r[cc][i]) * alpha[i]);
         }
+        tmem_st16(w.tmem_lane + ocol + S::kN * mb + w.h0, r[0]);
+        tmem_st16(w.tmem_lane + ocol + S::kN * mb + G + w.h0, r[1]);
     }
     tmem_wait_st();
 }
@@ -711,7 +722,7 @@ __device__ __forceinline__ bool half_reduce_writer(int lane) { return V == 16 ||
 template <int G, bool E>
 __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, int seg_hi, int head0) {
     using S = Shape<G>;
-    constexpr int kHL = S::kHL;
+    constexpr int kHL = 8;                          // heads per lane
     float* red = reinterpret_cast<float*>(w.base + kOffRed);
     float* lsum = reinterpret_cast<float*>(w.base + kOffLsum);
     int* vote = reinterpret_cast<int*>(w.base + kOffFlag);
@@ -755,19 +766,14 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
             fence_after_sync();
             // the warp's 16 token rows sit in lanes 0-15 of its TMEM quadrant:
-            // threads 0-15 read heads 0 .. G/2 - 1 of their row, threads 16-31
-            // heads G/2 .. G - 1 of the same row (term 1 at column h, term 2 at
-            // column G + h)
+            // threads 0-15 read heads h0 .. h0 + 7 of their row, threads 16-31
+            // heads h0 + 8 .. h0 + 15 of the same row (term 1 at column h,
+            // term 2 at column G + h)
             float s[kHL];
             {
                 uint32_t r1[kHL], r2[kHL];
-                if constexpr (kHL == 8) {
-                    tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot, r1);
-                    tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot + G, r2);
-                } else {
-                    tmem_ld_half16<kHL>(w.tmem_lane + kColS + S::kN * slot, r1);
-                    tmem_ld_half16<kHL>(w.tmem_lane + kColS + S::kN * slot + G, r2);
-                }
+                tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot + w.h0, r1);
+                tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot + G + w.h0, r2);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < kHL; ++j)
@@ -791,15 +797,15 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             // the running maximum moves only if some score got more than
             // 2^kTau above it (one vote per warp, then one barrier)
             need = __any_sync(0xffffffffu, need);
-            int* vb = vote + (i & 1) * 4;
+            int* vb = vote + w.wg * 8 + (i & 1) * 4;
             if (w.lane == 0) vb[w.wq] = need;
-            wg_bar();
+            wg_bar(w.wg);
             need = vb[0] | vb[1] | vb[2] | vb[3];
             if (need) {
                 const float hmax = half_reduce<true, kHL>(s, w.lane);
                 float* rb = red + (i & 1) * 4 * G;
                 if (half_reduce_writer<kHL>(w.lane)) rb[w.wq * G + w.hb + half_reduce_index<kHL>(w.lane)] = hmax;
-                wg_bar();
+                wg_bar(w.wg);
                 float alpha[kHL];
 #pragma unroll
                 for (int j = 0; j < kHL; ++j) {
@@ -812,8 +818,9 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                 }
                 if (it > 0) {
                     // O holds tiles up to i - 1: rescale once PV(i - 1) has landed;
-                    // every lane needs all G heads' factors (lanes 0 and 16 have them)
-                    float a_all[G];
+                    // every lane needs the warpgroup's 16 factors (lanes 0 and 16
+                    // have them)
+                    float a_all[16];
 #pragma unroll
                     for (int j = 0; j < kHL; ++j) {
                         a_all[j] = __shfl_sync(0xffffffffu, alpha[j], 0);
@@ -853,13 +860,8 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             // [P1;P2]^T: 16-head column group g = term * (G / 16) + head / 16
             uint8_t* pb = pbase + slot * S::kPBytes + (w.hb / 16) * kPUnit + w.srow * 16 + (w.hb % 16);
             uint8_t* pb2 = pb + (G / 16) * kPUnit;
-            if constexpr (kHL == 8) {
-                *reinterpret_cast<uint2*>(pb) = make_uint2(pk1[0], pk1[1]);
-                *reinterpret_cast<uint2*>(pb2) = make_uint2(pk2[0], pk2[1]);
-            } else {
-                *reinterpret_cast<uint4*>(pb) = make_uint4(pk1[0], pk1[1], pk1[2], pk1[3]);
-                *reinterpret_cast<uint4*>(pb2) = make_uint4(pk2[0], pk2[1], pk2[2], pk2[3]);
-            }
+            *reinterpret_cast<uint2*>(pb) = make_uint2(pk1[0], pk1[1]);
+            *reinterpret_cast<uint2*>(pb2) = make_uint2(pk2[0], pk2[1]);
             fence_proxy_async_smem();
             fence_before_sync();                    // orders a rescale's TMEM stores too
             mbar_arrive(&w.bars[P_FULL + slot]);
@@ -870,12 +872,13 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             const float hsum = half_reduce<false, kHL>(l, w.lane);
             if (half_reduce_writer<kHL>(w.lane)) lsum[w.wq * G + w.hb + half_reduce_index<kHL>(w.lane)] = hsum;
         }
-        wg_bar();
-        float inv[G];
+        wg_bar(w.wg);
+        float inv[16];                              // the warpgroup's heads h0 + t
 #pragma unroll
-        for (int h = 0; h < G; ++h) {
+        for (int t = 0; t < 16; ++t) {
+            const int h = w.h0 + t;
             const float L = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
-            inv[h] = L > 0.f ? p.k_scale / L : 0.f;
+            inv[t] = L > 0.f ? p.k_scale / L : 0.f;
         }
         float Lmine[kHL];                           // this lane's heads, for the lse
 #pragma unroll
@@ -883,7 +886,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             const int h = w.hb + j;
             Lmine[j] = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
         }
-        wg_bar();                                   // lsum is reused by the next segment
+        wg_bar(w.wg);                               // lsum is reused by the next segment
         const int jl = i - 1;                       // the segment's last tile
         mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
@@ -904,35 +907,29 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         const float lse_off = -kTau;                 // kPScale = 2^kTau
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
-            float o[G];
-#pragma unroll
-            for (int c = 0; c < S::kN / 16; c += 2) {     // two loads in flight per wait
+            float o[16];                            // heads h0 .. h0 + 15
+            {
                 uint32_t r[2][16];
-                tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c, r[0]);
-                tmem_ld16(w.tmem_lane + ocol + S::kN * mb + 16 * c + 16, r[1]);
+                tmem_ld16(w.tmem_lane + ocol + S::kN * mb + w.h0, r[0]);
+                tmem_ld16(w.tmem_lane + ocol + S::kN * mb + G + w.h0, r[1]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc)
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int h = (16 * (c + cc)) % G + t;
-                        o[h] = 16 * (c + cc) < G ? __uint_as_float(r[cc][t]) : o[h] + __uint_as_float(r[cc][t]);
-                    }
+                for (int t = 0; t < 16; ++t) o[t] = __uint_as_float(r[0][t]) + __uint_as_float(r[1][t]);
             }
             const int ch = mb * 128 + w.row;
             if (sg.part < 0) {
-                uint16_t* out = p.out + int64_t(row0) * kDCkv + ch;
+                uint16_t* out = p.out + (int64_t(row0) + w.h0) * kDCkv + ch;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    if (h >= nrows) break;
-                    out[h * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[h] * inv[h]));
+                for (int t = 0; t < 16; ++t) {
+                    if (w.h0 + t >= nrows) break;
+                    out[t * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[t] * inv[t]));
                 }
             } else {
-                float* po = p.part_o + (int64_t(sg.part) * p.part_rows + prow0) * kDCkv + ch;
+                float* po = p.part_o + (int64_t(sg.part) * p.part_rows + prow0 + w.h0) * kDCkv + ch;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    if (h >= nrows) break;
-                    po[h * kDCkv] = o[h] * inv[h];
+                for (int t = 0; t < 16; ++t) {
+                    if (w.h0 + t >= nrows) break;
+                    po[t * kDCkv] = o[t] * inv[t];
                 }
             }
         }
@@ -952,9 +949,10 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
 // 152 registers at G = 16 (no spills): with 3 warps per SM sub-partition
 // that leaves room for one warp of the q split kernel beside the CTA, so the
 // programmatic launch places decode CTAs while the split still runs (at 160
-// registers they waited for the split to drain; measured on GB300).
+// registers they waited for the split to drain; measured on GB300).  At
+// G = 32 the CTA runs 512 threads (two softmax warpgroups) at 128 registers.
 template <int G, bool E>
-__global__ void __maxnreg__(G == 16 ? 152 : 168) mla_decode_tc_kernel(const DecodeParams p) {
+__global__ void __maxnreg__(G == 16 ? 152 : 128) mla_decode_tc_kernel(const DecodeParams p) {
     using S = Shape<G>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -964,15 +962,28 @@ __global__ void __maxnreg__(G == 16 ? 152 : 168) mla_decode_tc_kernel(const Deco
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        // KV_FULL: 32 cp.async arrivals from each fill warp; SL_EMPTY: the fill
-        // warps and the four softmax warps
-        const uint32_t counts[SL_FULL] = {32 * kFillWarps, 32 * kFillWarps, 32 * kFillWarps,
-                                          32 * kFillWarps, 1, 1, 1, 1, 1, 1, 128, 128, 128, 128,
-                                          1, 1, 128, 128, 1, 1, 129, 129, 2};
-        for (int b = 0; b < SL_FULL; ++b) mbar_init(&bars[b], counts[b]);
+        // KV_FULL: 32 cp.async arrivals from each fill warp; KV_EMPTY, S_FULL,
+        // PV_DONE, Q_FULL: one commit or bulk-copy arrival; S_FREE, P_FULL,
+        // O_FREE: every softmax thread; Q_FREE: those and the QK commit; DONE:
+        // both MMA threads; SL_EMPTY: the fill warps and the softmax warps
+        constexpr uint32_t kSm = 128 * S::kWgs;
+        for (int b = 0; b < kStages; ++b) {
+            mbar_init(&bars[KV_FULL + b], 32 * kFillWarps);
+            mbar_init(&bars[KV_EMPTY + b], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars[S_FULL + b], 1);
+            mbar_init(&bars[S_FREE + b], kSm);
+            mbar_init(&bars[P_FULL + b], kSm);
+            mbar_init(&bars[PV_DONE + b], 1);
+            mbar_init(&bars[O_FREE + b], kSm);
+            mbar_init(&bars[Q_FULL + b], 1);
+            mbar_init(&bars[Q_FREE + b], kSm + 1);
+        }
+        mbar_init(&bars[DONE], 2);
         for (int e = 0; e < kRing; ++e) {
             mbar_init(&bars[SL_FULL + e], 1);
-            mbar_init(&bars[SL_EMPTY + e], kFillWarps + 4);
+            mbar_init(&bars[SL_EMPTY + e], kFillWarps + 4 * S::kWgs);
         }
         *abort = 0;
         mbar_fence_init();
@@ -985,11 +996,11 @@ __global__ void __maxnreg__(G == 16 ? 152 : 168) mla_decode_tc_kernel(const Deco
     const int seg_lo = p.cta_ptr[blockIdx.x], seg_hi = p.cta_ptr[blockIdx.x + 1];
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
-    if (warp == kWarpSched) {
+    if (warp == S::kWarpSched) {
         scheduler<E>(p, base, bars, abort, seg_lo, seg_hi, lane);
     } else if (warp < kFillWarps) {
         fill_warp<E>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
-    } else if (warp == kWarpMma || warp == kWarpPv) {
+    } else if (warp == kWarpMma || warp == S::kWarpPv) {
         if (lane == 0) {
             MmaCtx c;
             c.sbase = smem_u32(base);
@@ -1005,7 +1016,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 168) mla_decode_tc_kernel(const Deco
         __syncwarp();
     } else if (warp == kWarpQ) {
         q_fetch<G, E>(p, base, bars, abort, seg_lo, seg_hi, lane);
-    } else {                                      // warps kWarpWg .. kWarpWg + 3
+    } else {                                      // warps S::kWarpWg ..: softmax warpgroups
         WgCtx w;
         w.base = base;
         w.bars = bars;
@@ -1015,8 +1026,10 @@ __global__ void __maxnreg__(G == 16 ? 152 : 168) mla_decode_tc_kernel(const Deco
         w.flags = p.flags;
         w.row = quad * 32 + lane;
         w.srow = quad * 16 + (lane & 15);
-        w.hb = (lane >> 4) * S::kHL;
-        w.wq = warp - kWarpWg;
+        w.wg = G == 16 ? 0 : (warp - S::kWarpWg) >> 2;
+        w.wq = (warp - S::kWarpWg) & 3;
+        w.h0 = 16 * w.wg;
+        w.hb = w.h0 + (lane >> 4) * 8;
         w.lane = lane;
         softmax_wg<G, E>(p, w, seg_lo, seg_hi, head0);
     }
@@ -1059,7 +1072,7 @@ cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int d
     // the decode kernel starts while the split runs: only its q warp waits
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, p.head_groups);         // token ranges x head groups
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Shape<G>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
