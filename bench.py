@@ -44,7 +44,7 @@ from mla_decode_attention_run_gb300 import accounting as A  # noqa: E402
 METRIC = "MLA FP8 decode µs/call & achieved HBM GB/s vs ~8 TB/s peak; decode step ms"
 HEADS, PAGE = 16, 1
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SOURCES = ["decode.cu", "decode_tc.cu", "tc.cuh", "common.cuh", "plan.h"]
+DECODE_SOURCES = ["decode_tc.cu", "decode_params.h", "plan.h", "tc.cuh", "common.cuh"]   # the tcgen05 decode kernel's sources
 
 
 # ------------------------------------------------------------------ helpers

@@ -447,11 +447,13 @@ mla_status_t install(mla_plan_t* plan, Schedule&& s, size_t* workspace_bytes, vo
         }
         p->dev_meta_cap = cap;
     }
-    p->off_cta = 0;
-    p->off_segs = s.num_ctas + 1;
-    p->off_merge = p->off_segs + s.segs.size();
-    p->off_blocks = p->off_merge + s.merge.size();
-    p->off_seg_pages = p->off_blocks + s.blocks.size();
+    // the 4-int records first, so that each starts on 16 bytes (one vector
+    // load per record on the device); cudaMalloc memory is 256-byte aligned
+    p->off_merge = 0;
+    p->off_segs = p->off_merge + s.merge.size();
+    p->off_blocks = p->off_segs + s.segs.size();
+    p->off_cta = p->off_blocks + s.blocks.size();
+    p->off_seg_pages = p->off_cta + s.num_ctas + 1;
     std::memcpy(p->pinned + p->off_cta, s.cta_ptr.data(), (s.num_ctas + 1) * sizeof(int32_t));
     if (!s.segs.empty())
         std::memcpy(p->pinned + p->off_segs, s.segs.data(), s.segs.size() * sizeof(int32_t));

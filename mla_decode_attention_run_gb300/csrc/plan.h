@@ -92,7 +92,7 @@ mla_status_t build_extend_schedule(const int32_t* qo_indptr, const int32_t* kv_i
 struct mla_plan {
     mla::Schedule sched;
     int device = -1;
-    int32_t* dev_meta = nullptr;      // cta_ptr | segs | merge (int32)
+    int32_t* dev_meta = nullptr;      // merge | segs | blocks | cta_ptr | seg_pages (int32)
     size_t dev_meta_cap = 0;          // elements
     int32_t* pinned = nullptr;        // staging for the upload
     size_t pinned_cap = 0;
