@@ -13,7 +13,7 @@ per KV head ("When a Faster Kernel Doesn't Speed Up Serving", section
 proprietary models; these seeded draws with the same shapes stand in for
 that traffic.
 
-Recipe (all draws with torch.Generator(seed = 1000 + config number), CPU):
+Recipe (all draws with torch.Generator(seed = 1000 + the workload's number), CPU):
   * latents c_kv / k_pe: normal with the config's std, drawn in fp32 and
     rounded to BF16; k_scale = absmax(latents) / 448 in fp32, except the tiny
     config (std 1, k_scale 1.0);
@@ -65,7 +65,7 @@ class Workload:
         return int(self.seq_lens.sum())
 
 
-# name -> (config number, B, H, contexts, page_size, latent std)
+# name -> (workload number (seed offset), B, H, contexts, page_size, latent std)
 CONFIGS = {
     "tiny": dict(number=1, batch=2, heads=4, lens=[17, 33], page_size=1, pool=128, std=1.0),
     "single": dict(number=2, batch=1, heads=16, lens=[4096], page_size=1, pool=POOL_SLOTS,
@@ -154,7 +154,7 @@ def make_workload(name: str, *, batch: int | None = None, heads: int | None = No
                     k_scale=float(k_scale), seed=seed)
 
 
-# name -> (config number, B, H, contexts, new tokens per request): extend
+# name -> (workload number (seed offset), B, H, contexts, new tokens per request): extend
 # steps.  The pages time the extend path's cast of the whole history (once
 # per layer and extend step) but give no chunk size; the readings here are a
 # prefill chunk of 256 new tokens over the decode workload's history law, and
