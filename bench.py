@@ -474,7 +474,7 @@ def run_ours(args, rank, world, local):
     return result
 
 
-def measure_configs(torch, M, dev, stream):
+def measure_configs(torch, M, dev, stream, names=("single", "large_head")):
     """The single-stream (1 x 4,096 tokens) and 128-head (128 x 32,768 tokens,
     page size 64, 2.4 GB pool) decode calls, each timed as a CUDA graph of
     back-to-back calls on pools of quantized N(0, 0.5) latents.  The
@@ -488,6 +488,8 @@ def measure_configs(torch, M, dev, stream):
             tflops_peak = float(json.load(f).get("bf16_tflops", 0)) or None
     res = {}
     for name, reps in (("single", 50), ("large_head", 4)):
+        if name not in names:
+            continue
         w = W.make_workload(name, latent_requests=[])
         B, H, ps = w.batch, w.heads, w.page_size
         pool = torch.empty((w.num_slots, W.D_ALL), dtype=torch.uint8, device=dev)
@@ -933,6 +935,8 @@ def main(argv=None):
     ap.add_argument("--proj-only", action="store_true",
                     help="time only the fused KV projection store against cuBLAS + store and "
                          "print its JSON (a diagnostic)")
+    ap.add_argument("--config", choices=["single", "large_head"],
+                    help="time only that decode configuration and print its JSON (a diagnostic)")
     ap.add_argument("--pools", type=int, default=8,
                     help="pools the extend timing rotates over (--extend-only)")
     args = ap.parse_args(argv)
@@ -949,6 +953,17 @@ def main(argv=None):
         res = measure_kv_proj(torch, M, torch.device("cuda", local), stream, layers=args.layers)
         if rank == 0:
             print(json.dumps({"kv_proj": res}), flush=True)
+        return
+    if args.config:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        import mla_decode_attention_run_gb300 as M
+        torch.cuda.set_device(local)
+        stream = torch.cuda.Stream()
+        res = measure_configs(torch, M, torch.device("cuda", local), stream, names=(args.config,))
+        if rank == 0:
+            print(json.dumps({"configs": res}), flush=True)
         return
     if args.extend_only:
         import torch
