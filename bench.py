@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -96,10 +97,17 @@ def measured_peaks():
 
 
 def decode_source_hash() -> str:
+    """Hash of the tcgen05 decode kernel's code: its sources with comments
+    and blank lines removed, so that an edit of a comment keeps the recorded
+    traffic valid and any change of code voids it."""
     h = hashlib.sha256()
     for name in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "mla_decode_attention_run_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mla_decode_attention_run_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        lines = [ln.rstrip() for ln in text.splitlines() if ln.strip()]
+        h.update("\n".join(lines).encode())
     return h.hexdigest()[:16]
 
 

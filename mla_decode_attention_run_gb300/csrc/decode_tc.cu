@@ -19,9 +19,9 @@
 // terms are stacked along N, so one MMA computes both partial products and
 // reads the cache tile once.
 //
-// Tile = 64 tokens = the QK^T MMA's M.  Per tile:
-//   S^T[64 x 32]   = K_tile[64 x 576] . [q1;q2]^T     18 MMAs, K-major A/B
-//   O^T[512 x 32] += V^T[512 x 64] . [P1;P2]^T        8 MMAs, MN-major A/B
+// Tile = 64 tokens = the QK^T MMA's M; N = 2G (two terms of G heads).  Per tile:
+//   S^T[64 x 2G]   = K_tile[64 x 576] . [q1;q2]^T     18 MMAs, K-major A/B
+//   O^T[512 x 2G] += V^T[512 x 64] . [P1;P2]^T        8 MMAs, MN-major A/B
 // A 64-token tile (36 KB) keeps four tiles in flight in 144 KB of shared
 // memory, which hides a tile's fill -> QK^T -> softmax -> PV round trip.
 // The same swizzled smem tile serves as K-major A (tokens x dims) and
@@ -44,8 +44,9 @@
 // one request, each with its own causal limit; the softmax hides the tokens
 // at or past a row's limit on the tiles that reach them.
 //
-// Warp roles (one CTA per SM, persistent over its token range):
-//   warp 11    publishes tiles ahead of the stage fills: resolves each row's
+// Warp roles (one CTA per SM, persistent over its token range; warp numbers
+// for G = 16, 384 threads, with G = 32's in brackets, 512 threads):
+//   warp 11 [7]  publishes tiles ahead of the stage fills: resolves each row's
 //              pool slot (or -1: past the context, outside the pool) into a
 //              small shared ring and has L2 prefetch the rows' cache lines,
 //              so the fills below read L2 rather than wait on DRAM;
@@ -56,16 +57,17 @@
 //              gather at the HBM rate, which neither fewer warps nor TMA
 //              tile::gather4 reach;
 //   warp 4     one thread issues the QK^T MMAs, tile after tile;
-//   warp 10    one thread issues the PV MMAs, so that PV of one tile never
+//   warp 10 [6]  one thread issues the PV MMAs, so that PV of one tile never
 //              waits behind QK^T of the next;
 //   warp 5     fetches each segment's [q1;q2] image, per-row score
 //              multipliers and causal limits, written by the q split kernel
 //              that precedes this one (double-buffered for G = 16);
-//   warps 6-9  online softmax of a token's G heads and the E4M3 split of P
-//              (an M = 64 accumulator puts a tile's rows in lanes 0-15 of
-//              each warp's TMEM lane quadrant; threads 0-15 take the first
-//              half of the heads, 16-31 the second), rescaling O when the
-//              maximum moves, and the epilogue (all lanes: lane = output
+//   warps 6-9 [8-11, 12-15]  one softmax warpgroup per 16 heads: online
+//              softmax of a token's heads and the E4M3 split of P (an M = 64
+//              accumulator puts a tile's rows in lanes 0-15 of each warp's
+//              TMEM lane quadrant; threads 0-15 take 8 of the warpgroup's
+//              heads, 16-31 the other 8), rescaling its heads' O columns when
+//              their maximum moves, and the epilogue (all lanes: lane = output
 //              channel).
 // Every mbarrier wait is bounded; on a timeout the CTA sets
 // MLA_FLAG_WAIT_TIMEOUT, drains its MMAs and copies, frees TMEM and exits.
