@@ -37,6 +37,31 @@ MLA_DEVINLINE uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Split-KV partials are written by the decode and read once by the merge at
+// the end of the call, while the call streams far more than L2 holds: the
+// decode stores them with L2 priority evict_last, the merge reads them with
+// evict_first (cache-policy operands covering every access they are given to).
+MLA_DEVINLINE uint64_t l2_policy(bool keep) {
+    uint64_t pol;
+    if (keep) asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(pol));
+    else asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    return pol;
+}
+MLA_DEVINLINE void st_f32_hint(float* ptr, float v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" :: "l"(ptr), "f"(v), "l"(pol) : "memory");
+}
+MLA_DEVINLINE float ld_f32_hint(const float* ptr, uint64_t pol) {
+    float v;
+    asm volatile("ld.global.L2::cache_hint.f32 %0, [%1], %2;\n" : "=f"(v) : "l"(ptr), "l"(pol));
+    return v;
+}
+MLA_DEVINLINE float4 ld_f32x4_hint(const float4* ptr, uint64_t pol) {
+    float4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;\n"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(ptr), "l"(pol));
+    return v;
+}
+
 // 16-byte async copy global -> shared.  src_bytes = 0 writes zeros and reads
 // nothing (used for masked rows).
 MLA_DEVINLINE void cp_async16(void* smem, const void* gmem, uint32_t src_bytes) {

@@ -413,6 +413,7 @@ mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int part_rows,
     }
     float m = -INFINITY, wsum = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint64_t once = l2_policy(false);         // each partial is read once
     for (int c = 0; c < n; c += kMergeBatch) {
         float l[kMergeBatch];
         float4 v[kMergeBatch];
@@ -422,8 +423,9 @@ mla_merge_kernel(const int32_t* __restrict__ merge, int n_merge, int part_rows,
             const int64_t pr = int64_t(first + (ok ? c + i : 0)) * part_rows + h;
             // a partial whose tokens the row cannot see (extend) has lse = -inf
             // and o = 0: weight 0
-            l[i] = ok ? part_lse[pr] : -INFINITY;
-            v[i] = ok ? reinterpret_cast<const float4*>(part_o + pr * kDCkv)[t] : make_float4(0.f, 0.f, 0.f, 0.f);
+            l[i] = ok ? ld_f32_hint(part_lse + pr, once) : -INFINITY;
+            v[i] = ok ? ld_f32x4_hint(reinterpret_cast<const float4*>(part_o + pr * kDCkv) + t, once)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         float mc = m;
 #pragma unroll

@@ -928,10 +928,11 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                 }
             } else {
                 float* po = p.part_o + (int64_t(sg.part) * p.part_rows + prow0 + w.h0) * kDCkv + ch;
+                const uint64_t keep = l2_policy(true);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     if (w.h0 + t >= nrows) break;
-                    po[t * kDCkv] = o[t] * inv[t];
+                    st_f32_hint(po + t * kDCkv, o[t] * inv[t], keep);
                 }
             }
         }
@@ -942,7 +943,11 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
 #pragma unroll
             for (int j = 0; j < kHL; ++j)
-                if (w.hb + j < nrows) dst[w.hb + j] = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
+                if (w.hb + j < nrows) {
+                    const float v = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
+                    if (sg.part < 0) dst[w.hb + j] = v;
+                    else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
+                }
         }
         ++k;
     }
