@@ -38,8 +38,9 @@ MLA_DEVINLINE uint32_t smem_u32(const void* p) {
 }
 
 // Split-KV partials are written by the decode and read once by the merge at
-// the end of the call, while the call streams far more than L2 holds: the
-// decode stores them with L2 priority evict_last, the merge reads them with
+// the end of the call, and query images are written by the q split and read
+// at each segment start, while the call streams far more than L2 holds: both
+// are stored with L2 priority evict_last; the merge reads the partials with
 // evict_first (cache-policy operands covering every access they are given to).
 MLA_DEVINLINE uint64_t l2_policy(bool keep) {
     uint64_t pol;
@@ -49,6 +50,10 @@ MLA_DEVINLINE uint64_t l2_policy(bool keep) {
 }
 MLA_DEVINLINE void st_f32_hint(float* ptr, float v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" :: "l"(ptr), "f"(v), "l"(pol) : "memory");
+}
+MLA_DEVINLINE void st_v4_hint(void* ptr, const uint4& v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;\n"
+                 :: "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol) : "memory");
 }
 MLA_DEVINLINE float ld_f32_hint(const float* ptr, uint64_t pol) {
     float v;

@@ -601,15 +601,16 @@ __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const Decode
     const int row1 = r, row2 = G + r;
     uint4 t1, t2;
     split_chunk(va, vb, scale, t1, t2);
+    const uint64_t keep = l2_policy(true);          // read again at each segment of the image
     {                                               // c_kv: 128-byte rows, 128-byte swizzle
         const int cb = lane >> 3, cc = lane & 7;
-        *reinterpret_cast<uint4*>(img + cb * S::kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4)) = t1;
-        *reinterpret_cast<uint4*>(img + cb * S::kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4)) = t2;
+        st_v4_hint(img + cb * S::kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4), t1, keep);
+        st_v4_hint(img + cb * S::kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4), t2, keep);
     }
     if (rope) {                                     // k_pe: 64-byte rows, 64-byte swizzle
         split_chunk(ra, rb, scale, t1, t2);
-        *reinterpret_cast<uint4*>(img + 4 * S::kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4)) = t1;
-        *reinterpret_cast<uint4*>(img + 4 * S::kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4)) = t2;
+        st_v4_hint(img + 4 * S::kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4), t1, keep);
+        st_v4_hint(img + 4 * S::kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4), t2, keep);
     }
     if (lane == 0) {
         reinterpret_cast<float*>(img + S::kQBytes)[r] =
