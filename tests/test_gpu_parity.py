@@ -184,6 +184,7 @@ def test_decode_large_head_full_size_sampled():
     (16, 64, [1, 4096, 130]),
     (32, 2, [300, 77]),
     (48, 1, [513]),
+    (64, 1, [2000, 5, 700, 64]),                   # 32-head CTAs in two head groups
     (128, 64, [1000, 64, 3]),
 ])
 def test_decode_edge_shapes(heads, ps, lens):
