@@ -349,7 +349,7 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": False,
-        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 mma (q and p as two e4m3 terms) / f32 accumulate",
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 mma (q as three e4m3 terms, p as two) / f32 accumulate",
         "data": "synthetic (seeded N(0,0.5) latents, N(0,1) q; no model weights)",
         "config": {"workload": workload_name, "batch": B, "heads": HEADS, "layers": L,
                    "page_size": PAGE, "pool_slots": P, "tokens_per_call": n_tok,

@@ -94,7 +94,7 @@ typedef struct mla_plan* mla_plan_t;
  *                   + t % page_size.
  *  kv_dtype         element type of the pools run() will read.
  *  workspace_bytes  out: device scratch run() needs: the split-KV partials
- *                   and, on the tensor-core FP8 path, one 18,560-byte image
+ *                   and, on the tensor-core FP8 path, one 27,840-byte image
  *                   of the split query per request and group of 16 heads.
  *  stream           the plan's device metadata is uploaded on this stream
  *                   (stream-ordered before later runs on it).
@@ -116,7 +116,14 @@ mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indptr_host,
  *     s_t = softmax_scale * sum_d q[b][h][d] * k_t[d]
  *     out[b][h] = sum_t softmax(s)_t * v_t        (BF16)
  *     lse[b][h] = ln sum_t exp(s_t)               (fp32, natural log)
- * A request with seq_len 0 gets out = 0 and lse = -inf.
+ * A request with seq_len 0 gets out = 0 and lse = -inf; a head whose query
+ * row holds an infinity or a NaN gets out = NaN and lse = NaN.
+ * Arithmetic of FP8 plans: the E4M3 cache bytes are the tensor-core operands
+ * as they are; each query row enters as three E4M3 terms (exactly for every
+ * entry above 2^-14 of the row's largest, with 4 significant bits below) and
+ * the softmax weights as two (8 significant bits; a token more than 19 log2
+ * units, about 13 nats, below the running maximum score may be dropped from
+ * the output sum, one more than 23 always is); products accumulate in fp32.
  *
  *  q                BF16, element (b, h, d) at q + b*q_stride_b + h*q_stride_h
  *                   + d (strides in elements; d < 576 contiguous).
@@ -167,7 +174,9 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q, int64_t q_stride_b,
  *  - The array exists once per GPU that loads the library and stays
  *    allocated until the process exits.
  *  - The first call on a device looks up the array's device address; make
- *    that first call before any stream capture begins.
+ *    that first call before any stream capture begins.  The address is kept
+ *    until exit: after a cudaDeviceReset of that device, do not use this
+ *    call on it again.
  *  - Every call shares the array: calls whose GPU work overlaps (other
  *    streams, other host threads) race on it.  Calls on one stream are
  *    ordered.  Nothing in the array needs to start at zero.
@@ -359,7 +368,9 @@ mla_status_t kv_proj_store_fp8(const void* x, int64_t x_row_stride, const void* 
  * kv_indices[j]*page_size + r, converted as
  *     BF16_rne(float(value(byte)) * k_scale)
  * (one fp32 multiply; with k_scale = 1 this is exactly the pages' unscaled
- * .to(bfloat16)).  A caller then replans with indices 0..n_pages-1 and runs a
+ * .to(bfloat16)).  The two NaN codes 0x7F / 0xFF become the quiet NaN
+ * 0x7FC0 (sign dropped, as PyTorch's float8_e4m3fn -> bfloat16 cast gives
+ * them).  A caller then replans with indices 0..n_pages-1 and runs a
  * MLA_KV_BF16 decode on the compact buffers.
  *  kv_indices  int32 [n_pages], device.
  *  ckv_out     BF16 [n_pages*page_size][512];  kpe_out  BF16 [..][64].
@@ -378,6 +389,22 @@ mla_status_t kv_gather_cast(const void* ckv_pool, int64_t ckv_row_stride_bytes,
  * MLA_ERR_CUDA if the synchronisation failed, else MLA_OK.
  */
 mla_status_t mla_get_last_error(void* stream, uint32_t* device_flags_out);
+
+/*
+ * mla_debug_set_wait_limit -- test hook for the decode kernels' failure
+ * handling.  Every wait of the FP8 decode / extend kernels on an in-kernel
+ * barrier is bounded: after the limit the CTA sets MLA_FLAG_WAIT_TIMEOUT,
+ * abandons its work (its outputs are void), lets its copies and MMAs
+ * finish, frees its tensor memory and exits, so a stuck pipeline never
+ * hangs the GPU ("When a Faster Kernel Doesn't Speed Up Serving" runs the
+ * decode inside CUDA graphs of a serving loop, where a hung kernel stalls
+ * every request).  The limit is 2 s; this call sets it, in nanoseconds, for
+ * the current device (0 restores 2 s).  A tiny limit makes the next calls
+ * give up at their first wait, which is how the timeout path is tested.
+ * Synchronous: call it between launches, with no decode kernel running.
+ * Errors: MLA_ERR_CUDA.
+ */
+mla_status_t mla_debug_set_wait_limit(uint64_t limit_ns);
 
 /* Static description of a status code. */
 const char* mla_status_string(mla_status_t status);

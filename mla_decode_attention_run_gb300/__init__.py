@@ -19,7 +19,7 @@ __all__ = [
     "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast", "mla_get_last_error",
     "exported_symbols", "D_CKV", "D_KPE", "D_QK", "mla_decode_run_static_scratch",
     "STATIC_SCRATCH_BYTES", "mla_extend_plan", "mla_extend_run", "mla_extend_schedule",
-    "kv_proj_store_fp8",
+    "kv_proj_store_fp8", "mla_debug_set_wait_limit",
 ]
 
 D_CKV, D_KPE, D_QK = 512, 64, 576
@@ -73,12 +73,14 @@ def library():
                                       _i64, _P, _P]
     lib.kv_gather_cast.argtypes = [_P, _i64, _P, _i64, _i64, _P, _i64, _i32, _f32, _P, _P, _P]
     lib.mla_get_last_error.argtypes = [_P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.mla_debug_set_wait_limit.argtypes = [ctypes.c_uint64]
     lib.mla_status_string.argtypes = [ctypes.c_int]
     lib.mla_status_string.restype = ctypes.c_char_p
     for name in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
                  "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
                  "mla_get_last_error", "mla_decode_run_static_scratch", "mla_extend_plan",
-                 "mla_extend_run", "mla_extend_schedule", "kv_proj_store_fp8"):
+                 "mla_extend_run", "mla_extend_schedule", "kv_proj_store_fp8",
+                 "mla_debug_set_wait_limit"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -92,7 +94,8 @@ def exported_symbols() -> list[str]:
     for n in ("mla_decode_plan", "mla_decode_run", "mla_decode_plan_destroy",
               "mla_decode_plan_info", "mla_decode_schedule", "kv_store_fp8", "kv_gather_cast",
               "mla_get_last_error", "mla_status_string", "mla_decode_run_static_scratch",
-              "mla_extend_plan", "mla_extend_run", "mla_extend_schedule", "kv_proj_store_fp8"):
+              "mla_extend_plan", "mla_extend_run", "mla_extend_schedule", "kv_proj_store_fp8",
+              "mla_debug_set_wait_limit"):
         getattr(lib, n)
         names.append(n)
     return names
@@ -324,3 +327,11 @@ def mla_get_last_error(stream=None) -> int:
     if st not in (0, 4):
         raise MLAError(st, "mla_get_last_error")
     return flags.value
+
+
+def mla_debug_set_wait_limit(limit_ns: int):
+    """Time limit (ns) of the decode kernels' bounded in-kernel waits on the
+    current device; 0 restores the default (2 s).  A test hook: a tiny limit
+    makes the next decode calls give up and set FLAG_WAIT_TIMEOUT."""
+    _check(library().mla_debug_set_wait_limit(ctypes.c_uint64(int(limit_ns))),
+           "mla_debug_set_wait_limit")

@@ -147,6 +147,11 @@ MLA_DEVINLINE uint32_t sub_f16x2(uint32_t a, uint32_t b) {
     asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
+MLA_DEVINLINE uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
 
 MLA_DEVINLINE uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;

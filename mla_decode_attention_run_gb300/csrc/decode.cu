@@ -612,3 +612,7 @@ extern "C" mla_status_t mla_extend_run(mla_plan_t plan, const void* q, int64_t q
                     seq_lens_dev, k_scale, softmax_scale, out, lse, workspace, workspace_bytes,
                     stream);
 }
+
+extern "C" mla_status_t mla_debug_set_wait_limit(uint64_t limit_ns) {
+    return mla::set_decode_wait_limit(limit_ns) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}

@@ -44,4 +44,8 @@ struct DecodeParams {
 // p.head_groups.
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream);
 
+// Sets the time limit of the tcgen05 decode kernels' bounded waits on the
+// current device (0: the default); synchronous.
+cudaError_t set_decode_wait_limit(uint64_t limit_ns);
+
 }  // namespace mla

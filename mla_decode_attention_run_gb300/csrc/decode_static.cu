@@ -30,7 +30,10 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up once per
 // device (the first call on a device does this; make that first call before
-// any stream capture begins).
+// any stream capture begins).  The address is kept for the life of the
+// process: a cudaDeviceReset of the device discards the array with the
+// context, so a process that resets a device must not use this call on it
+// afterwards.
 mla_status_t scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;

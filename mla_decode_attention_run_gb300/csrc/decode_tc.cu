@@ -13,14 +13,16 @@
 // written as the sum of two E4M3 numbers, q * 2^sigma = q1 + q2 (q1 the
 // nearest E4M3, q2 the nearest E4M3 to the remainder); a BF16 value has 8
 // significant bits and each term carries 4, so the sum is exact whenever both
-// terms are normal -- anything smaller than 2^-14 of the head's largest entry
-// may lose bits, far below the output's BF16 rounding.  Likewise the softmax
-// weights p * 16 = p1 + p2 (8 significant bits, like a BF16 P).  The two
-// terms are stacked along N, so one MMA computes both partial products and
-// reads the cache tile once.
+// terms are normal, i.e. for every entry above 2^-14 of the head's largest.
+// What those two terms miss of smaller entries (E4M3's range is only 2^17)
+// goes into a third term q3 at its own, finer power-of-two scale, with 4
+// significant bits.  Likewise the softmax weights p * 16 = p1 + p2 / 2^5 (8
+// significant bits, like a BF16 P; the second term scaled up so that weights
+// far below the maximum survive).  The terms are stacked along N, so one MMA
+// computes all partial products and reads the cache tile once.
 //
-// Tile = 64 tokens = the QK^T MMA's M; N = 2G (two terms of G heads).  Per tile:
-//   S^T[64 x 2G]   = K_tile[64 x 576] . [q1;q2]^T     18 MMAs, K-major A/B
+// Tile = 64 tokens = the QK^T MMA's M.  Per tile:
+//   S^T[64 x 3G]   = K_tile[64 x 576] . [q1;q2;q3]^T  18 MMAs, K-major A/B
 //   O^T[512 x 2G] += V^T[512 x 64] . [P1;P2]^T        8 MMAs, MN-major A/B
 // A 64-token tile (36 KB) keeps four tiles in flight in 144 KB of shared
 // memory, which hides a tile's fill -> QK^T -> softmax -> PV round trip.
@@ -59,7 +61,7 @@
 //   warp 4     one thread issues the QK^T MMAs, tile after tile;
 //   warp 10 [6]  one thread issues the PV MMAs, so that PV of one tile never
 //              waits behind QK^T of the next;
-//   warp 5     fetches each segment's [q1;q2] image, per-row score
+//   warp 5     fetches each segment's [q1;q2;q3] image, per-row score
 //              multipliers and causal limits, written by the q split kernel
 //              that precedes this one (double-buffered for G = 16);
 //   warps 6-9 [8-11, 12-15]  one softmax warpgroup per 16 heads: online
@@ -102,6 +104,9 @@ constexpr float kTau = 4.f;                 // lazy-rescale threshold (log2 unit
 constexpr float kPScale = 16.f;             // P is stored as p * 2^kTau
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kP2Scale = 32.f;            // P's second term is stored x 2^5
+constexpr uint32_t kP2ScaleF16x2 = 0x50005000u;   // 32.0 in both f16 halves
+constexpr int kCoefBytesPerRow = 12;        // per q image row: two fp32 multipliers, one int32 limit
 constexpr int kRing = 8;                    // published tiles' slot lists (and L2 prefetches) in flight
 static_assert(kRing > kStages, "the ring covers the tiles the stages hold");
 
@@ -111,9 +116,10 @@ constexpr int kMaxG = 32;
 
 template <int G>
 struct Shape {
-    static constexpr int kN = 2 * G;                  // MMA N: both E4M3 terms of G heads
-    static constexpr int kQBlk = kN * 128;            // q rows x 128 B per 128-channel block
-    static constexpr int kQBytes = 4 * kQBlk + kN * 64;   // + the k_pe block
+    static constexpr int kN = 2 * G;                  // PV MMA N: both E4M3 terms of P for G heads
+    static constexpr int kNq = 3 * G;                 // QK^T MMA N: the three E4M3 terms of q
+    static constexpr int kQBlk = kNq * 128;           // q rows x 128 B per 128-channel block
+    static constexpr int kQBytes = 4 * kQBlk + kNq * 64;  // + the k_pe block
     static constexpr int kQBufs = G == 16 ? 2 : 1;    // q buffers in shared memory
     static constexpr int kOBufs = G == 16 ? 2 : 1;    // O accumulators in TMEM
     static constexpr int kPBytes = (kN / 16) * kPUnit;    // [P1;P2]^T of one tile
@@ -124,8 +130,12 @@ struct Shape {
     static constexpr int kWarpWg = G == 16 ? 6 : 8;   // first softmax warp
     static constexpr int kWarpPv = G == 16 ? 10 : 6;
     static constexpr int kWarpSched = G == 16 ? 11 : 7;
-    static constexpr uint32_t kColO = 2 * kN;         // TMEM: S[0], S[1], then O[b] + 4 kN b
-    static constexpr int kImage = kQBytes + G * 8;    // q image + score multipliers + causal limits
+    // TMEM: S[0], S[1] (kNq columns each, starting on multiples of 32), then
+    // O[b] at kColO + 4 kN b
+    static constexpr uint32_t kSCols = (kNq + 31) / 32 * 32;
+    static constexpr uint32_t kColO = 2 * kSCols;
+    // q image + two score multipliers and a causal limit per row
+    static constexpr int kImage = kQBytes + G * kCoefBytesPerRow;
     static_assert(kQBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
     static_assert(kColO + kOBufs * 4 * kN <= kTmemCols, "TMEM columns");
 };
@@ -142,11 +152,12 @@ constexpr int kOffRing = kOffP + 2 * Shape<kMaxG>::kPBytes;   // kRing x 64 slot
 constexpr int kOffBar = kOffRing + kRing * kTT * 4;
 constexpr int kOffRed = kOffBar + 512;      // tile maxima: 2 x 4 warps x G
 constexpr int kOffLsum = kOffRed + 2 * 4 * kMaxG * 4;   // softmax denominators: 4 warps x G
-constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // per q buffer: G multipliers, G limits
-constexpr int kOffFlag = kOffCoef + 2 * 16 * 8;         // rescale votes: per warpgroup 2 x 4 warps
+constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // per q buffer: 2 G multipliers, G limits
+constexpr int kOffFlag = kOffCoef + 2 * 16 * kCoefBytesPerRow;   // rescale votes: per warpgroup 2 x 4 warps
 constexpr int kOffMisc = kOffFlag + 64;     // TMEM base, abort flag
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-static_assert(Shape<16>::kQBufs * 16 * 8 <= 2 * 16 * 8 && Shape<32>::kQBufs * 32 * 8 <= 2 * 16 * 8,
+static_assert(Shape<16>::kQBufs * 16 * kCoefBytesPerRow <= 2 * 16 * kCoefBytesPerRow &&
+                  Shape<32>::kQBufs * 32 * kCoefBytesPerRow <= 2 * 16 * kCoefBytesPerRow,
               "multiplier and limit space");
 static_assert(Shape<16>::kImage == kTcQImageBytes && Shape<32>::kImage == 2 * kTcQImageBytes,
               "q image sizes the plan reserves");
@@ -218,6 +229,14 @@ __device__ __forceinline__ void wg_bar(int g) {
 // in) L2, so a stage is held for an L2 round trip rather than a DRAM one.
 
 constexpr int32_t kNoRow = INT32_MIN;
+
+// A wait made by every lane of a warp that then acts together (shuffles,
+// warp barriers): the warp goes on only if every lane's wait succeeded, so
+// that after an abort no lane leaves the loop while the others stay in it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* flags) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, flags));
+}
 
 // Cursor over the tiles of a CTA's segments, with the raw page entries of
 // rows 2 lane, 2 lane + 1 of one tile.
@@ -324,7 +343,7 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
         int32_t sl[2];
         cur.rows(p, sl);
         cur.advance(p, lane);                         // the next tile's index loads fly meanwhile
-        if (!mbar_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
+        if (!warp_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             if (sl[q] < 0) continue;
@@ -351,13 +370,13 @@ __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
         const int slot = i % kStages;
         const uint32_t u = static_cast<uint32_t>(i / kStages);
         const int e = i % kRing;
-        if (!mbar_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, abort, p.flags)) break;
+        if (!warp_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, abort, p.flags)) break;
         int32_t sl[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[SL_EMPTY + e]);
-        if (!mbar_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
+        if (!warp_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
         fill_share(p, base + kOffStage + slot * kStage, sl, w, lane);
         mbar_arrive_cp_async(&bars[KV_FULL + slot]);
     }
@@ -394,7 +413,7 @@ __device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
     const uint64_t b128 = smem_desc(qb, 16, 1024, kSwizzle128B);
     const uint64_t a64 = smem_desc(stage + 4 * kBlk, 16, 512, kSwizzle64B);
     const uint64_t b64 = smem_desc(qb + 4 * S::kQBlk, 16, 512, kSwizzle64B);
-    const uint32_t d = c.tmem + kColS + S::kN * slot;
+    const uint32_t d = c.tmem + kColS + S::kSCols * slot;
 #pragma unroll
     for (int ks = 0; ks < kKSteps; ++ks) {
         const uint64_t a = ks < 16 ? desc_at(a128, (ks >> 2) * kBlk + (ks & 3) * 32)
@@ -515,14 +534,24 @@ __device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
 // ---------------------------------------------------------------- q prep
 //
 // q is split once per request by a small kernel that runs just before the
-// decode kernel: it writes [q1;q2] as the exact shared-memory image the QK^T
-// MMA reads (128-byte swizzle for the 512 c_kv channels, 64-byte for the 64
-// k_pe channels) plus the per-head score multipliers.  A decode CTA then
+// decode kernel: it writes [q1;q2;q3] as the exact shared-memory image the
+// QK^T MMA reads (128-byte swizzle for the 512 c_kv channels, 64-byte for the
+// 64 k_pe channels) plus the per-head score multipliers.  A decode CTA then
 // fetches a segment's q with two bulk copies.
+//
+// Per head, with x = q * 2^sigma (largest |x| in [128, 256)):
+//   q1 = E4M3(x), q2 = E4M3(x - q1)           -- exact for every entry above
+//                                                2^-14 of the head's largest
+//   r  = x - q1 - q2 (exact in fp32),  q3 = E4M3(r * 2^tau)
+//                                              (largest |r| 2^tau in [128, 256))
+// so q = 2^-sigma (q1 + q2) + 2^-(sigma + tau) q3: entries the first two terms
+// cannot hold (too small next to the head's largest) keep 4 significant bits
+// in the third, down to 2^-14 of the largest such remainder.
 
-// Splits 16 BF16 values (two uint4) scaled by `scale` into two E4M3 terms.
+// Splits 16 BF16 values (two uint4) scaled by `scale` into two E4M3 terms
+// and returns the exact remainders in `rem`.
 __device__ __forceinline__ void split_chunk(const uint4& va, const uint4& vb, float scale, uint4& t1,
-                                            uint4& t2) {
+                                            uint4& t2, float (&rem)[16]) {
     const uint32_t w8[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
     uint32_t o1[4], o2[4];
 #pragma unroll
@@ -535,7 +564,11 @@ __device__ __forceinline__ void split_chunk(const uint4& va, const uint4& vb, fl
             const float x1 = __uint_as_float(w & 0xffff0000u) * scale;
             const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
             const float2 d = e4m3x2_to_float2(b1);
-            const uint16_t b2 = f32x2_to_e4m3x2(x0 - d.x, x1 - d.y);
+            const float y0 = x0 - d.x, y1 = x1 - d.y;    // exact
+            const uint16_t b2 = f32x2_to_e4m3x2(y0, y1);
+            const float2 d2 = e4m3x2_to_float2(b2);
+            rem[4 * e + 2 * hh] = y0 - d2.x;             // exact
+            rem[4 * e + 2 * hh + 1] = y1 - d2.y;
             lo1 |= static_cast<uint32_t>(b1) << (16 * hh);
             lo2 |= static_cast<uint32_t>(b2) << (16 * hh);
         }
@@ -546,6 +579,16 @@ __device__ __forceinline__ void split_chunk(const uint4& va, const uint4& vb, fl
     t2 = make_uint4(o2[0], o2[1], o2[2], o2[3]);
 }
 
+// 16 remainders times `scale` -> one E4M3 term.
+__device__ __forceinline__ uint4 third_term(const float (&rem)[16], float scale) {
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        o[e] = static_cast<uint32_t>(f32x2_to_e4m3x2(rem[4 * e] * scale, rem[4 * e + 1] * scale)) |
+               (static_cast<uint32_t>(f32x2_to_e4m3x2(rem[4 * e + 2] * scale, rem[4 * e + 3] * scale)) << 16);
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __device__ __forceinline__ float amax_bf16x8(const uint4& v, float a) {
     const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -554,15 +597,43 @@ __device__ __forceinline__ float amax_bf16x8(const uint4& v, float a) {
     return a;
 }
 
+// true if one of the 8 BF16 values is an infinity or a NaN (exponent all ones)
+__device__ __forceinline__ bool nonfinite_bf16x8(const uint4& v) {
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) bad |= (w4[e] & 0x7F80u) == 0x7F80u || (w4[e] & 0x7F800000u) == 0x7F800000u;
+    return bad;
+}
+
+__device__ __forceinline__ float amax_f32x16(const float (&r)[16], float a) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) a = fmaxf(a, fabsf(r[i]));
+    return a;
+}
+
+// 2^e with e clamped to [-100, 100] (scales of the q terms)
+__device__ __forceinline__ int split_exponent(float amax) {
+    int e2 = 0;
+    frexpf(amax, &e2);                              // amax = m * 2^e2, m in [0.5, 1)
+    const int s = amax > 0.f ? 8 - e2 : 0;          // amax * 2^s in [128, 256)
+    return s > 100 ? 100 : (s < -100 ? -100 : s);
+}
+
 constexpr int kSplitThreads = 64;
 
 // One warp per image row: lane c splits 16-channel chunk c of c_kv, lanes 0-3
 // also chunk c of k_pe.  Decode: one image per (request, group of G heads);
-// heads >= H get zero rows and multiplier 0.  Extend: one image per query
+// heads >= H get zero rows and multipliers 0.  Extend: one image per query
 // block, row r = block row r (token row / H, head row % H); rows past the
-// block's end are zero.  Each valid row also gets its causal limit.
+// block's end are zero.  Each valid row also gets its causal limit.  A row
+// holding an infinity or a NaN gets zero terms and NaN multipliers: its
+// output row and lse come out NaN.
+// At most 56 registers: one warp of it then fits on an SM sub-partition
+// beside a 16-head decode CTA (3 warps of 152 registers), so the decode
+// kernel's CTAs are placed while the split still runs.
 template <int G>
-__global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const DecodeParams p) {
+__global__ void __maxnreg__(56) mla_q_split_kernel(const DecodeParams p) {
     using S = Shape<G>;
     griddep_launch_dependents();                // the decode kernel may start loading KV now
     const int wg = (blockIdx.x * kSplitThreads + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -586,36 +657,51 @@ __global__ void __launch_bounds__(kSplitThreads) mla_q_split_kernel(const Decode
     const uint4* src =
         reinterpret_cast<const uint4*>(p.q + tok * p.q_sb + int64_t(valid ? head : 0) * p.q_sh);
     const uint4 z = make_uint4(0, 0, 0, 0);
-    const uint4 va = valid ? src[2 * lane] : z, vb = valid ? src[2 * lane + 1] : z;
+    uint4 va = valid ? src[2 * lane] : z, vb = valid ? src[2 * lane + 1] : z;
     const bool rope = lane < 4;
-    const uint4 ra = valid && rope ? src[64 + 2 * lane] : z, rb = valid && rope ? src[64 + 2 * lane + 1] : z;
+    uint4 ra = valid && rope ? src[64 + 2 * lane] : z, rb = valid && rope ? src[64 + 2 * lane + 1] : z;
+    const bool bad = __any_sync(0xffffffffu, nonfinite_bf16x8(va) || nonfinite_bf16x8(vb) ||
+                                                 nonfinite_bf16x8(ra) || nonfinite_bf16x8(rb));
+    if (bad) va = vb = ra = rb = z;
     float amax = amax_bf16x8(rb, amax_bf16x8(ra, amax_bf16x8(vb, amax_bf16x8(va, 0.f))));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    int e2 = 0;
-    frexpf(amax, &e2);                              // amax = m * 2^e2, m in [0.5, 1)
-    int sigma = amax > 0.f ? 8 - e2 : 0;            // max |q| * 2^sigma in [128, 256)
-    sigma = sigma > 100 ? 100 : (sigma < -100 ? -100 : sigma);
+    const int sigma = split_exponent(amax);
     const float scale = ldexpf(1.f, sigma);
+    uint4 c1, c2, k1, k2;
+    float rc[16], rk[16];
+    split_chunk(va, vb, scale, c1, c2, rc);
+    split_chunk(ra, rb, scale, k1, k2, rk);          // zeros on lanes 4-31
+    float amax3 = amax_f32x16(rk, amax_f32x16(rc, 0.f));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax3 = fmaxf(amax3, __shfl_xor_sync(0xffffffffu, amax3, o));
+    const int tau = amax3 > 0.f ? split_exponent(amax3) : 0;
+    const float scale3 = ldexpf(1.f, tau);
+    const uint4 c3 = third_term(rc, scale3), k3 = third_term(rk, scale3);
+
     uint8_t* img = p.qimg + int64_t(image) * S::kImage;
-    const int row1 = r, row2 = G + r;
-    uint4 t1, t2;
-    split_chunk(va, vb, scale, t1, t2);
+    const int row1 = r, row2 = G + r, row3 = 2 * G + r;
     const uint64_t keep = l2_policy(true);          // read again at each segment of the image
     {                                               // c_kv: 128-byte rows, 128-byte swizzle
         const int cb = lane >> 3, cc = lane & 7;
-        st_v4_hint(img + cb * S::kQBlk + row1 * 128 + ((cc ^ (row1 & 7)) << 4), t1, keep);
-        st_v4_hint(img + cb * S::kQBlk + row2 * 128 + ((cc ^ (row2 & 7)) << 4), t2, keep);
+        uint8_t* blk = img + cb * S::kQBlk;
+        st_v4_hint(blk + row1 * 128 + ((cc ^ (row1 & 7)) << 4), c1, keep);
+        st_v4_hint(blk + row2 * 128 + ((cc ^ (row2 & 7)) << 4), c2, keep);
+        st_v4_hint(blk + row3 * 128 + ((cc ^ (row3 & 7)) << 4), c3, keep);
     }
     if (rope) {                                     // k_pe: 64-byte rows, 64-byte swizzle
-        split_chunk(ra, rb, scale, t1, t2);
-        st_v4_hint(img + 4 * S::kQBlk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4), t1, keep);
-        st_v4_hint(img + 4 * S::kQBlk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4), t2, keep);
+        uint8_t* blk = img + 4 * S::kQBlk;
+        st_v4_hint(blk + row1 * 64 + ((lane ^ ((row1 >> 1) & 3)) << 4), k1, keep);
+        st_v4_hint(blk + row2 * 64 + ((lane ^ ((row2 >> 1) & 3)) << 4), k2, keep);
+        st_v4_hint(blk + row3 * 64 + ((lane ^ ((row3 >> 1) & 3)) << 4), k3, keep);
     }
     if (lane == 0) {
-        reinterpret_cast<float*>(img + S::kQBytes)[r] =
-            valid ? ldexpf(p.softmax_scale * p.k_scale * kLog2e, -sigma) : 0.f;
-        reinterpret_cast<int32_t*>(img + S::kQBytes)[G + r] = valid ? lim : 0;
+        // multipliers of the first two terms and of the third (2^-tau finer)
+        const float base = valid ? (bad ? __int_as_float(0x7FC00000) : p.softmax_scale * p.k_scale * kLog2e) : 0.f;
+        float* coef = reinterpret_cast<float*>(img + S::kQBytes);
+        coef[r] = ldexpf(base, -sigma);
+        coef[G + r] = ldexpf(ldexpf(base, -sigma), -tau);
+        reinterpret_cast<int32_t*>(coef + 2 * G)[r] = valid ? lim : 0;
     }
 }
 
@@ -634,11 +720,23 @@ __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, vo
         const int qs = k % S::kQBufs;
         const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
         if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
+        // After an abort the softmax warps keep arriving on Q_FREE without
+        // the QK^T commit, so a phase can complete before the buffer's last
+        // copy has landed; a second copy (and arrive.expect_tx) on Q_FULL
+        // then would overrun its phase.  So no copy is issued once the CTA
+        // has aborted, and none before the buffer's previous copy landed
+        // (its own Q_FULL phase: immediate unless aborted).
+        if (*abort) break;
+        if (k >= S::kQBufs) {
+            volatile int never = 0;
+            if (!mbar_wait(&bars[Q_FULL + qs], (qu - 1) & 1, &never, p.flags, 1000000000ull)) break;
+        }
         const int64_t image = E ? sg.b : int64_t(sg.b) * p.head_groups + blockIdx.y;
         const uint8_t* img = p.qimg + image * S::kImage;
         mbar_arrive_expect_tx(&bars[Q_FULL + qs], S::kImage);
         bulk_copy_g2s(smem_u32(base + kOffQ + qs * S::kQBytes), img, S::kQBytes, &bars[Q_FULL + qs]);
-        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * G * 8), img + S::kQBytes, G * 8, &bars[Q_FULL + qs]);
+        bulk_copy_g2s(smem_u32(base + kOffCoef + qs * G * kCoefBytesPerRow), img + S::kQBytes,
+                      G * kCoefBytesPerRow, &bars[Q_FULL + qs]);
         ++k;
     }
     // copies in flight (after an abort) land before the CTA exits
@@ -745,8 +843,9 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags);
         // the segment's score multipliers and causal limits stay in shared
         // memory (its q buffer is released at the end of the segment)
-        const float* coef = coefs + qs * 2 * G;
-        const int32_t* lim = reinterpret_cast<const int32_t*>(coef + G);
+        const float* coef = coefs + qs * 3 * G;      // first two terms' multipliers
+        const float* coef3 = coef + G;                  // the third term's
+        const int32_t* lim = reinterpret_cast<const int32_t*>(coef + 2 * G);
         // extend: tiles reaching the first row's limit need the causal mask
         // (rows are in token order, so the first row's limit is the lowest)
         const int mask_from = E ? lim[0] : INT32_MAX;
@@ -774,13 +873,17 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             // term 2 at column G + h)
             float s[kHL];
             {
-                uint32_t r1[kHL], r2[kHL];
-                tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot + w.h0, r1);
-                tmem_ld_half8<kHL>(w.tmem_lane + kColS + S::kN * slot + G + w.h0, r2);
+                uint32_t r1[kHL], r2[kHL], r3[kHL];
+                const uint32_t sc = w.tmem_lane + kColS + S::kSCols * slot + w.h0;
+                tmem_ld_half8<kHL>(sc, r1);
+                tmem_ld_half8<kHL>(sc + G, r2);
+                tmem_ld_half8<kHL>(sc + 2 * G, r3);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < kHL; ++j)
-                    s[j] = valid ? (__uint_as_float(r1[j]) + __uint_as_float(r2[j])) * coef[w.hb + j] : -INFINITY;
+                    s[j] = valid ? fmaf(__uint_as_float(r1[j]) + __uint_as_float(r2[j]), coef[w.hb + j],
+                                        __uint_as_float(r3[j]) * coef3[w.hb + j])
+                                 : -INFINITY;
             }
             fence_before_sync();
             mbar_arrive(&w.bars[S_FREE + slot]);
@@ -847,11 +950,15 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                     const int j = 4 * e2 + 2 * hh;
                     const float x0 = m[j] == -INFINITY ? 0.f : fast_exp2(s[j] - m[j]) * kPScale;
                     const float x1 = m[j + 1] == -INFINITY ? 0.f : fast_exp2(s[j + 1] - m[j + 1]) * kPScale;
-                    // x = p1 + p2: p1 the nearest E4M3, p2 the nearest E4M3 to
-                    // the remainder, taken in f16 (x <= 256 keeps 11 bits there,
-                    // and f16(x) - p1 is exact); the denominator sums x itself
+                    // x = p1 + p2 / 2^5: p1 the nearest E4M3, p2 the nearest
+                    // E4M3 to 2^5 times the remainder, taken in f16 (x <= 256
+                    // keeps 11 bits there, f16(x) - p1 is exact and at most 8,
+                    // and the factor 2^5 is exact); the denominator sums x
+                    // itself.  The factor keeps weights down to 2^-15 / 16
+                    // of the running maximum's in the second term.
                     const uint16_t b1 = f32x2_to_e4m3x2(x0, x1);
-                    const uint16_t b2 = f16x2_to_e4m3x2(sub_f16x2(pack_f16x2(x0, x1), e4m3x2_to_f16x2(b1)));
+                    const uint16_t b2 = f16x2_to_e4m3x2(
+                        mul_f16x2(sub_f16x2(pack_f16x2(x0, x1), e4m3x2_to_f16x2(b1)), kP2ScaleF16x2));
                     l[j] += x0;
                     l[j + 1] += x1;
                     w1 |= static_cast<uint32_t>(b1) << (16 * hh);
@@ -881,13 +988,15 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         for (int t = 0; t < 16; ++t) {
             const int h = w.h0 + t;
             const float L = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
-            inv[t] = L > 0.f ? p.k_scale / L : 0.f;
+            // a head whose q held an infinity or a NaN has NaN multipliers:
+            // its output and lse become NaN (nothing else of it is NaN)
+            inv[t] = (L > 0.f ? p.k_scale / L : 0.f) + (coef[h] - coef[h]);
         }
         float Lmine[kHL];                           // this lane's heads, for the lse
 #pragma unroll
         for (int j = 0; j < kHL; ++j) {
             const int h = w.hb + j;
-            Lmine[j] = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
+            Lmine[j] = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h] + (coef[h] - coef[h]);
         }
         wg_bar(w.wg);                               // lsum is reused by the next segment
         const int jl = i - 1;                       // the segment's last tile
@@ -917,7 +1026,8 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                 tmem_ld16(w.tmem_lane + ocol + S::kN * mb + G + w.h0, r[1]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int t = 0; t < 16; ++t) o[t] = __uint_as_float(r[0][t]) + __uint_as_float(r[1][t]);
+                for (int t = 0; t < 16; ++t)
+                    o[t] = fmaf(__uint_as_float(r[1][t]), 1.f / kP2Scale, __uint_as_float(r[0][t]));
             }
             const int ch = mb * 128 + w.row;
             if (sg.part < 0) {
@@ -1013,7 +1123,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128) mla_decode_tc_kernel(const Deco
             MmaCtx c;
             c.sbase = smem_u32(base);
             c.tmem = tmem;
-            c.idesc_qk = idesc_e4m3_f32(kTT, S::kN, false, false);
+            c.idesc_qk = idesc_e4m3_f32(kTT, S::kNq, false, false);
             c.idesc_pv = idesc_e4m3_f32(128, S::kN, true, true);   // M = 128 channels of a block
             c.bars = bars;
             c.abort = abort;
@@ -1092,6 +1202,11 @@ cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int d
 }
 
 }  // namespace
+
+cudaError_t set_decode_wait_limit(uint64_t limit_ns) {
+    const uint64_t v = limit_ns ? limit_ns : kDefaultWaitLimitNs;
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+}
 
 cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
     int dev = 0;

@@ -12,6 +12,7 @@
 namespace mla {
 namespace {
 
+constexpr uint32_t kBf16QuietNaN = 0x7FC0u;
 constexpr int kStoreUnitsPerRow = (kDCkv + kDKpe) / 8;   // 8 elements per thread
 constexpr int kGatherUnitsPerRow = (kDCkv + kDKpe) / 16; // 16 bytes per thread
 
@@ -94,7 +95,12 @@ kv_gather_cast_kernel(const uint8_t* __restrict__ ckv_pool, int64_t ckv_stride,
             for (int h = 0; h < 2; ++h) {
                 const uint32_t f16x2 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> (16 * h)));
                 const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&f16x2));
-                o[2 * q + h] = pack_bf16x2(__fmul_rn(f.x, k_scale), __fmul_rn(f.y, k_scale));
+                uint32_t v = pack_bf16x2(__fmul_rn(f.x, k_scale), __fmul_rn(f.y, k_scale));
+                // the NaN codes 0x7F / 0xFF give the quiet NaN 0x7FC0 whatever
+                // their sign, as PyTorch's float8_e4m3fn -> bfloat16 cast does
+                if (f.x != f.x) v = (v & 0xFFFF0000u) | kBf16QuietNaN;
+                if (f.y != f.y) v = (v & 0x0000FFFFu) | (kBf16QuietNaN << 16);
+                o[2 * q + h] = v;
             }
         }
         uint4* d = reinterpret_cast<uint4*>(dst);

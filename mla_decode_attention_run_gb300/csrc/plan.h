@@ -19,10 +19,11 @@ constexpr int kTcTileTokens = 64;
 // balances tiles + this per segment across CTAs
 constexpr int kTcSegmentCost = 2;
 constexpr int kHeadsPerCta = 16;
-// tcgen05 path: per request, [q1;q2] as the shared-memory image the MMA reads
-// (2 x 16 rows x 576 E4M3, swizzled) followed by 16 fp32 score multipliers and
-// 16 int32 causal limits (extend: a row sees the tokens before its limit)
-constexpr int kTcQImageBytes = 2 * kHeadsPerCta * 576 + kHeadsPerCta * 8;
+// tcgen05 path: per request and group of 16 heads, [q1;q2;q3] as the
+// shared-memory image the MMA reads (3 x 16 rows x 576 E4M3, swizzled)
+// followed by 2 x 16 fp32 score multipliers and 16 int32 causal limits
+// (extend: a row sees the tokens before its limit)
+constexpr int kTcQImageBytes = 3 * kHeadsPerCta * 576 + kHeadsPerCta * 12;
 
 // Which decode kernel a plan launches.
 enum class DecodeKernel : int32_t {

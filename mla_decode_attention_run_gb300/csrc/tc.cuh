@@ -24,6 +24,8 @@ namespace tc {
 
 // ------------------------------------------------------------- descriptors
 
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;
+
 enum Swizzle : uint64_t { kSwizzleNone = 0, kSwizzle128B = 2, kSwizzle64B = 4, kSwizzle32B = 6 };
 
 // Shared-memory matrix descriptor (sm_100 tcgen05 format).
@@ -178,18 +180,6 @@ MLA_DEVINLINE void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
                  :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-// TMA gather of four rows (row coordinates r0..r3, starting column x) of a
-// 2-D tensor map into consecutive box rows at `dst`; completes on `bar`.
-MLA_DEVINLINE void tma_gather4(uint32_t dst, const void* tensor_map, int32_t x, int32_t r0,
-                               int32_t r1, int32_t r2, int32_t r3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n"
-        :: "r"(dst), "l"(tensor_map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-           "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Bulk copy of `bytes` (a multiple of 16) from 16-byte aligned global memory
 // to 16-byte aligned shared memory; completes as transaction bytes on `bar`.
 MLA_DEVINLINE void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -248,12 +238,21 @@ MLA_DEVINLINE uint64_t global_ns() {
     return t;
 }
 
+namespace {
+// Default time limit of a bounded wait, in ns: one copy per translation unit
+// that includes this header.  mla_debug_set_wait_limit changes the decode
+// kernels' copy (tests use it to make a wait give up).
+__device__ uint64_t g_wait_limit_ns = kDefaultWaitLimitNs;
+}  // namespace
+
 // Waits for the phase with the given parity to complete.  Gives up after
-// `limit_ns` (or at once if *abort is already set), sets *abort and the
-// MLA_FLAG_WAIT_TIMEOUT flag, and returns false.
+// `limit_ns` (0: the default limit above), or at once if *abort is already
+// set; on giving up it sets *abort and the MLA_FLAG_WAIT_TIMEOUT flag and
+// returns false.
 MLA_DEVINLINE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags,
-                             uint64_t limit_ns = 2000000000ull) {
+                             uint64_t limit_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (limit_ns == 0) limit_ns = g_wait_limit_ns;
     const uint64_t t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -70,6 +70,6 @@ def check_attention(out: torch.Tensor, lse: torch.Tensor, o_ref: np.ndarray,
         f"{where}: output error {np.abs(o - o_ref)[worst]:.3e} at {worst} "
         f"(ref {o_ref[worst]:.4f}, got {o[worst]:.4f})")
     both_inf = np.isneginf(l) & np.isneginf(lse_ref)
-    dl = np.where(both_inf, 0.0, np.abs(l - lse_ref))
+    dl = np.abs(np.where(both_inf, 0.0, l) - np.where(both_inf, 0.0, lse_ref))
     assert np.all(dl <= LSE_TOL), f"{where}: lse error {np.nanmax(dl):.3e}"
     return float(np.abs(o - o_ref).max(initial=0)), float(dl.max(initial=0))

@@ -91,6 +91,30 @@ def test_gather_cast_bitexact(page_size, k_scale):
     assert np.array_equal(bf16_bits(kp), ref_kpe)
 
 
+@pytest.mark.parametrize("page_size,k_scale", [(1, 1.0), (3, 0.37), (1, 2.0 ** -7)])
+def test_gather_cast_bitexact_on_every_byte_including_nan(page_size, k_scale):
+    """Pools holding all 256 byte values, the NaN codes 0x7F and 0xFF
+    included, in every channel position: bit-exact with the oracle (NaN ->
+    0x7FC0)."""
+    g = np.random.default_rng(41)
+    pages = 120
+    rows = pages * page_size
+    pool0 = ((np.arange(rows * 576, dtype=np.int64) * 7 + 3) % 256).astype(np.uint8).reshape(rows, 576)
+    pool0 = pool0[g.permutation(rows)]
+    assert np.count_nonzero((pool0 & 0x7F) == 0x7F) > 100
+    idx = g.permutation(pages)[:97].astype(np.int32)
+    ref_ckv, ref_kpe = oracle.kv_gather_cast(pool0[:, :512], pool0[:, 512:], idx, page_size,
+                                             k_scale)
+    pool = torch.from_numpy(pool0).cuda()
+    n = idx.size * page_size
+    ck = torch.empty(n, 512, dtype=torch.bfloat16, device="cuda")
+    kp = torch.empty(n, 64, dtype=torch.bfloat16, device="cuda")
+    M.kv_gather_cast(pool[:, :512], pool[:, 512:], dev_i32(idx), page_size, k_scale, ck, kp)
+    assert M.mla_get_last_error() == 0
+    assert np.array_equal(bf16_bits(ck), ref_ckv)
+    assert np.array_equal(bf16_bits(kp), ref_kpe)
+
+
 def test_gather_cast_equals_torch_cast_at_unit_scale():
     """With k_scale = 1 the gather-cast of every page equals the pages'
     full-pool .to(bfloat16) restricted to those rows."""

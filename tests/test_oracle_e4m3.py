@@ -196,3 +196,28 @@ def test_float_to_bf16_matches_torch():
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle.float_to_bf16(x)
     assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("k_scale", [1.0, 0.37, 2.0 ** -7])
+def test_gather_cast_all_256_bytes_including_nan(k_scale):
+    """Every byte value, the two NaN codes included.  At k_scale = 1 the
+    oracle is PyTorch's float8_e4m3fn -> bfloat16 cast bit for bit (the
+    pages' .to(bfloat16); it gives the quiet NaN 0x7FC0 for 0x7F and 0xFF).
+    At any other scale the finite bytes follow one fp32 multiply and a BF16
+    rounding, and the NaN codes still give 0x7FC0."""
+    rows = np.arange(256 * 9, dtype=np.int64).reshape(-1, 576) % 256
+    pool = rows.astype(np.uint8)                    # 4 rows, each byte value 9 times
+    idx = np.arange(pool.shape[0], dtype=np.int32)
+    ckv, kpe = oracle.kv_gather_cast(pool[:, :512], pool[:, 512:], idx, 1, k_scale)
+    got = np.concatenate([ckv, kpe], axis=1)
+    f8 = torch.from_numpy(pool).view(torch.float8_e4m3fn)
+    nan = (pool & 0x7F) == 0x7F
+    assert nan.sum() == 2 * 9
+    assert np.all(got[nan] == 0x7FC0)
+    if k_scale == 1.0:
+        ref = f8.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got, ref)
+    else:
+        ref = (f8.float() * torch.tensor(k_scale, dtype=torch.float32)).to(torch.bfloat16)
+        ref = ref.view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got[~nan], ref[~nan])

@@ -29,7 +29,12 @@ def _built():
     M.mla_get_last_error()
 
 
-def _close(out, lse, ref_out, ref_lse):
+def _identical(out, lse, ref_out, ref_lse):
+    """Both calls run the same deterministic kernels on the same plan and
+    inputs, only with the scratch elsewhere: the results agree bit for bit
+    (which is also within the attention tolerance the other tests use)."""
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), ref_lse.view(torch.int32))
     o, r = out.float().cpu().numpy(), ref_out.float().cpu().numpy()
     assert np.all(np.abs(o - r) <= ATOL + RTOL * np.abs(r))
     assert np.all(np.abs(lse.cpu().numpy() - ref_lse.cpu().numpy()) <= LSE_TOL)
@@ -56,24 +61,26 @@ def test_static_scratch_matches_workspace_call_twice_in_a_row():
         M.mla_decode_run_static_scratch(plan, q, ckv, kpe, w.num_slots, indptr, idx, lens,
                                         w.k_scale, w.softmax_scale, out, lse)
         assert M.mla_get_last_error() == 0
-        _close(out, lse, ref_out, ref_lse)
+        _identical(out, lse, ref_out, ref_lse)
     M.mla_decode_plan_destroy(plan)
 
 
 def test_static_scratch_refuses_plans_that_need_more():
-    """A plan whose partials exceed the array is refused with status 3 before
-    any launch.  Of the two shapes tried, the 128-head, 128 x 32,768-token
-    one needs more than the array on a 152-SM GPU and the small one fits."""
+    """A plan whose scratch exceeds the array is refused with status 3 before
+    any launch, and one that fits is accepted.  The plan's scratch depends on
+    the GPU's SM count, so which of the two shapes needs more is read from
+    the plans (on a 152-SM GPU the 128-head, 128 x 32,768-token one does)."""
     tiny = torch.zeros(64, 576, dtype=torch.uint8, device="cuda")
     q = torch.zeros(128, 128, 576, dtype=torch.bfloat16, device="cuda")
     out = torch.zeros(128, 128, 512, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(128, 128, dtype=torch.float32, device="cuda")
-    refused = 0
+    refused = expected = 0
     for lens, heads, ps in (([32768] * 128, 128, 64), ([5000, 3000], 16, 1)):
         lens = np.asarray(lens, np.int32)
         indptr = np.zeros(len(lens) + 1, np.int32)
         indptr[1:] = np.cumsum((lens + ps - 1) // ps)
         plan = M.mla_decode_plan(indptr, lens, len(lens), heads, ps)
+        expected += plan.workspace_bytes > M.STATIC_SCRATCH_BYTES
         if plan.workspace_bytes > M.STATIC_SCRATCH_BYTES:
             with pytest.raises(M.MLAError) as e:
                 M.mla_decode_run_static_scratch(plan, q[:len(lens), :heads], tiny[:, :512],
@@ -84,4 +91,4 @@ def test_static_scratch_refuses_plans_that_need_more():
             assert e.value.status == 3
             refused += 1
         M.mla_decode_plan_destroy(plan)
-    assert refused == 1
+    assert refused == expected >= 1
