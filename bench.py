@@ -240,15 +240,56 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     dist = init_dist(world, "nccl")
-    L, B, P = args.layers, args.batch, W.POOL_SLOTS
-    w, indptr, idx, lens, new_slots = step_page_table(B)
-    n_tok = int(lens.sum())
+    L, P = args.layers, W.POOL_SLOTS
 
-    # ---- resident state: pools, per-layer q and new-token latents, outputs
+    # ---- resident state: 78 pools with latents in the headline batch's
+    # active slots (per-layer k_scale = absmax / 448 of those latents)
     pools = torch.empty(L, P, 576, dtype=torch.uint8, device=dev)
+    w = step_page_table(args.batch)[0]
     active_d = torch.from_numpy(w.kv_indices.astype(np.int64)).to(dev)
     k_scales = fill_pools(torch, M, pools, active_d, L, seed=5)
-    gq = torch.Generator(device=dev).manual_seed(77)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    result = measure_step(torch, M, args, args.batch, pools, k_scales, stream, dist, world, local,
+                          headline=True)
+    # the single-stream step: the same 78 pools, latents stored into its own
+    # active slots with each layer's k_scale
+    if args.batch != 1 and not args.no_batch1:
+        w1 = step_page_table(1)[0]
+        g1 = torch.Generator(device=dev).manual_seed(4097)
+        slots1 = torch.from_numpy(w1.kv_indices.astype(np.int64)).to(dev)
+        for l in range(L):
+            lat = (torch.randn(slots1.numel(), 576, generator=g1, device=dev) * 0.5).to(torch.bfloat16)
+            M.kv_store_fp8(lat[:, :512].contiguous(), lat[:, 512:].contiguous(), slots1,
+                           k_scales[l], pools[l, :, :512], pools[l, :, 512:])
+        torch.cuda.synchronize()
+        result["decode_step_b1"] = measure_step(torch, M, args, 1, pools, k_scales, stream, dist,
+                                                world, local, headline=False)
+
+    # ---- the other configurations' decode call, timed alone (rank 0)
+    if rank == 0 and not args.no_configs:
+        result["configs"] = measure_configs(torch, M, dev, stream)
+        result["extend"] = measure_extend(torch, M, dev, stream)
+        result["kv_proj"] = measure_kv_proj(torch, M, dev, stream)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.no_configs:
+        result["cpu_oracle_configs"] = oracle_timings()
+    return result
+
+
+def measure_step(torch, M, args, B, pools, k_scales, stream, dist, world, local, headline):
+    """The full decode step at batch B over the resident pools: host plan +
+    a CUDA graph of 78 x (kv_store_fp8 of the new token, mla_decode_run);
+    the 78 decode calls alone (value: us per call); the same through host
+    buffers (e2e); the two cast baselines and the category ledger; the CPU
+    oracle on one layer's call.  headline: the benchmark line's own keys
+    (and its launch count); otherwise the same figures as a sub-dict."""
+    dev = pools.device
+    L, P = args.layers, W.POOL_SLOTS
+    rank = dist.get_rank() if dist is not None else 0
+    w, indptr, idx, lens, new_slots = step_page_table(B)
+    n_tok = int(lens.sum())
+    gq = torch.Generator(device=dev).manual_seed(77 if headline else 77 + 1000 + B)
     q = torch.randn(L, B, HEADS, 576, generator=gq, device=dev).to(torch.bfloat16)
     new_ckv = (torch.randn(L, B, 512, generator=gq, device=dev) * 0.5).to(torch.bfloat16)
     new_kpe = (torch.randn(L, B, 64, generator=gq, device=dev) * 0.5).to(torch.bfloat16)
@@ -260,7 +301,6 @@ def run_ours(args, rank, world, local):
     slots_d = torch.from_numpy(new_slots).to(dev)
     sm_scale = W.SOFTMAX_SCALE
 
-    stream = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         plan = M.mla_decode_plan(indptr, lens, B, HEADS, PAGE, M.MLA_KV_FP8_E4M3, stream=stream)
@@ -345,16 +385,19 @@ def run_ours(args, rank, world, local):
     peak, peak_src = measured_peaks()
     workload_name = f"decode_step_b{B}_h{HEADS}_l{L}"
 
-    result = {
-        "metric": METRIC, "value": round(us_per_call, 3), "unit": "us/call",
+    result = {} if not headline else {"metric": METRIC}
+    result.update({
+        "value": round(us_per_call, 3), "unit": "us/call",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 mma (q as three e4m3 terms, p as two) / f32 accumulate",
         "data": "synthetic (seeded N(0,0.5) latents, N(0,1) q; no model weights)",
         "config": {"workload": workload_name, "batch": B, "heads": HEADS, "layers": L,
                    "page_size": PAGE, "pool_slots": P, "tokens_per_call": n_tok,
-                   "contexts": "uniform[1024,8192] + 1 appended", "parallelism": "replicas",
-                   "l2": "inputs larger than L2 (78 pools, ~8.4 GB touched per step)",
+                   "contexts": ("4096" if B == 1 else "uniform[1024,8192]") + " + 1 appended",
+                   "parallelism": "replicas",
+                   "l2": "inputs larger than L2 (78 pools, %.2f GB touched per step)" % (
+                       L * n_tok * 576 / 1e9),
                    "graphs": "CUDA graph per step; plan rebuilt on the host each step"},
         "decode_step_ms": round(ms_per_step, 4),
         "tokens_per_s": round(B * world / (ms_per_step * 1e-3), 1),
@@ -370,7 +413,16 @@ def run_ours(args, rank, world, local):
                      "traffic_of": "mla_decode_tc_kernel (ncu, profiles/decode_traffic.json)",
                      "algorithmic_bytes_per_launch": call_bytes,
                      "peak_source": f"{peak_src} HBM copy bandwidth"},
-    }
+    })
+    if not headline:
+        for k in ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                  "vs_baseline", "dtype", "data", "gpu_launches"):
+            result.pop(k, None)
+        if L * n_tok * 576 < 3 * 129e6:
+            result["config"]["l2"] = ("%d layers x %.1f MB of active rows per step (%.2f GB): "
+                                      "about L2's size, so part of each call's rows may still be "
+                                      "in L2 from the previous step" % (L, n_tok * 576 / 1e6,
+                                                                        L * n_tok * 576 / 1e9))
 
     # ---- e2e through the public API from pinned host buffers
     h_q = torch.empty_like(q, device="cpu").pin_memory()
@@ -454,7 +506,7 @@ def run_ours(args, rank, world, local):
 
     # ---- the two baselines the pages describe, per decode step
     if not args.no_baselines:
-        base = run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, store,
+        base = run_baselines(torch, M, args, B, stream, pools, q, out, lse, ws, k_scales, store,
                              indptr, idx, lens, timed, dist, dev)
         ledger = base.pop("ledger")
         # the fused step's graph (store + decode per layer) without the host plan
@@ -465,18 +517,10 @@ def run_ours(args, rank, world, local):
         result["baselines"] = base
         result["ledger"] = ledger
 
-    # ---- the other configurations' decode call, timed alone (rank 0)
-    if rank == 0 and not args.no_configs:
-        result["configs"] = measure_configs(torch, M, dev, stream)
-        result["extend"] = measure_extend(torch, M, dev, stream)
-        result["kv_proj"] = measure_kv_proj(torch, M, dev, stream)
-
-    # ---- CPU oracle baseline (rank 0, one GPU)
+    # ---- CPU oracle baseline (rank 0, one GPU): one layer's call of this step
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_from_device(pools[0], q[0], indptr, idx, lens,
-                                                          k_scales[0])
-        if not args.no_configs:
-            result["cpu_oracle_configs"] = oracle_timings()
+                                                          k_scales[0], B)
     del g_step, g_decode
     M.mla_decode_plan_destroy(plan)
     return result
@@ -718,9 +762,9 @@ def category_ledger(step_ms, parts):
     return out
 
 
-def run_baselines(torch, M, args, stream, pools, q, out, lse, ws, k_scales, store, indptr, idx,
+def run_baselines(torch, M, args, B, stream, pools, q, out, lse, ws, k_scales, store, indptr, idx,
                   lens, timed, dist, dev):
-    L, B, P = args.layers, args.batch, W.POOL_SLOTS
+    L, P = args.layers, W.POOL_SLOTS
     n = idx.size
     idx_d = torch.from_numpy(idx).to(dev)
     indptr_d = torch.from_numpy(indptr).to(dev)
@@ -879,7 +923,7 @@ def oracle_timings():
     return res
 
 
-def cpu_baseline_from_device(pool_d, q_d, indptr, idx, lens, k_scale):
+def cpu_baseline_from_device(pool_d, q_d, indptr, idx, lens, k_scale, batch):
     import oracle
     import torch
     pool_np = pool_d.cpu().numpy()
@@ -887,7 +931,7 @@ def cpu_baseline_from_device(pool_d, q_d, indptr, idx, lens, k_scale):
     threads = oracle.max_threads()
     dt = oracle_call(pool_np, q_bits, indptr, idx, lens, k_scale)
     return {"value": round(dt * 1e6, 1), "unit": "us/call", "cores": threads, "kind": "oracle",
-            "sample": "one layer's full decode call (batch 40, 16 heads, all contexts), "
+            "sample": f"one layer's full decode call (batch {batch}, 16 heads, all contexts), "
                       "C fp64 oracle with OpenMP over (request, head)"}
 
 
@@ -937,6 +981,8 @@ def main(argv=None):
     ap.add_argument("--no-baselines", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--no-batch1", action="store_true",
+                    help="skip the batch-1 (single-stream) decode step")
     ap.add_argument("--extend-only", action="store_true",
                     help="time only the extend workloads and print their JSON (a diagnostic, "
                          "not the benchmark line)")

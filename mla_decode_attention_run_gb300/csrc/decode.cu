@@ -544,7 +544,9 @@ mla_status_t run_plan(mla_plan_t plan, bool extend, const void* q, int64_t q_str
 
     if (s.kernel == DecodeKernel::kTc && num_pool_slots >= INT32_MAX) return MLA_ERR_UNSUPPORTED;
     if (s.num_ctas > 0 && s.kernel == DecodeKernel::kTc) {
-        if (launch_decode_tc(p, s.num_ctas, cs) != cudaSuccess) return MLA_ERR_CUDA;
+        // each range's segments and first segment travel with the launch
+        // (kept in the plan: built once per plan, reused by every run)
+        if (launch_decode_tc(p, plan->ranges, s.num_ctas, cs) != cudaSuccess) return MLA_ERR_CUDA;
     } else if (s.num_ctas > 0) {
         const dim3 grid(s.num_ctas * s.head_groups);
         cudaError_t e;

@@ -39,10 +39,23 @@ struct DecodeParams {
     int32_t n_blocks;
 };
 
+// The tcgen05 decode's token ranges (its CTAs, per head group), passed by
+// value as a kernel parameter: a CTA then knows its segments and issues its
+// first page-table loads at once instead of after two dependent global loads
+// (range -> segment record -> page entries).  Ranges past kMaxTcRanges read
+// the plan's device tables instead.
+constexpr int kMaxTcRanges = 256;
+struct TcRanges {
+    int32_t n;                          // ranges described here
+    int32_t seg[kMaxTcRanges + 1];      // range c: segments [seg[c], seg[c + 1])
+    int4 first[kMaxTcRanges];           // range c's first segment: t0, t1, page-table offset, 0
+};
+
 // Launches the q split kernel and then, as its programmatic dependent, the
 // tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` token ranges x
 // p.head_groups.
-cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, const TcRanges& ranges, int grid,
+                             cudaStream_t stream);
 
 // Sets the time limit of the tcgen05 decode kernels' bounded waits on the
 // current device (0: the default); synchronous.

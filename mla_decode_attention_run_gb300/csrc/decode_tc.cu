@@ -248,9 +248,22 @@ struct TileCursor {
     int32_t pg[2];                      // page entry, or kNoRow past the context
     int32_t t[2];                       // token index of each row
 
-    __device__ void init(const DecodeParams& p, int lo, int hi, int lane) {
+    // first: the first segment's t0, t1 and page-table offset when the
+    // launch carries them (its page entries are then requested before the
+    // segment record arrives), else nullptr
+    __device__ void init(const DecodeParams& p, int lo, int hi, const int4* first, int lane) {
         si = lo;
         seg_hi = hi;
+        if (first != nullptr && si < seg_hi) {
+            pages = p.indices + first->z;
+            sg.t0 = first->x;
+            sg.t1 = first->y;
+            it = 0;
+            prefetch(p, lane);
+            sg = load_seg<E>(p, si);
+            if (sg.ntiles > 0) return;
+            ++si;
+        }
         seek(p, lane);
     }
     // Moves to the first segment from si on that has tiles and requests its
@@ -327,14 +340,13 @@ __device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage
     }
 }
 
+// cur: started by the caller (its first page entries already requested)
 template <bool E>
 __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                          int seg_lo, int seg_hi, int lane) {
+                          TileCursor<E>& cur, int lane) {
     int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
     // one prefetch sweep per row when k_pe follows c_kv in the same row
     const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
-    TileCursor<E> cur;
-    cur.init(p, seg_lo, seg_hi, lane);
     // publishes every tile as soon as its ring entry is free (the ring bounds
     // how far ahead of the softmax warps the prefetches run)
     for (int n = 0; cur.valid(); ++n) {
@@ -1070,7 +1082,8 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
 // registers they waited for the split to drain; measured on GB300).  At
 // G = 32 the CTA runs 512 threads (two softmax warpgroups) at 128 registers.
 template <int G, bool E>
-__global__ void __maxnreg__(G == 16 ? 152 : 128) mla_decode_tc_kernel(const DecodeParams p) {
+__global__ void __maxnreg__(G == 16 ? 152 : 128)
+    mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TcRanges ranges) {
     using S = Shape<G>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -1078,6 +1091,12 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128) mla_decode_tc_kernel(const Deco
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + kOffMisc);
     volatile int* abort = reinterpret_cast<volatile int*>(base + kOffMisc + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool ranged = static_cast<int>(blockIdx.x) < ranges.n;
+    const int seg_lo = ranged ? ranges.seg[blockIdx.x] : p.cta_ptr[blockIdx.x];
+    const int seg_hi = ranged ? ranges.seg[blockIdx.x + 1] : p.cta_ptr[blockIdx.x + 1];
+    // the scheduler requests its first page entries while the CTA sets up
+    TileCursor<E> cur;
+    if (warp == S::kWarpSched) cur.init(p, seg_lo, seg_hi, ranged ? &ranges.first[blockIdx.x] : nullptr, lane);
 
     if (tid == 0) {
         // KV_FULL: 32 cp.async arrivals from each fill warp; KV_EMPTY, S_FULL,
@@ -1111,11 +1130,10 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128) mla_decode_tc_kernel(const Deco
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int seg_lo = p.cta_ptr[blockIdx.x], seg_hi = p.cta_ptr[blockIdx.x + 1];
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == S::kWarpSched) {
-        scheduler<E>(p, base, bars, abort, seg_lo, seg_hi, lane);
+        scheduler<E>(p, base, bars, abort, cur, lane);
     } else if (warp < kFillWarps) {
         fill_warp<E>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
     } else if (warp == kWarpMma || warp == S::kWarpPv) {
@@ -1164,7 +1182,8 @@ std::mutex g_mu;
 std::vector<char> g_attr;     // per device: bit (G / 16 - 1) + 2 E: max dynamic smem set
 
 template <int G, bool E>
-cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int dev) {
+cudaError_t launch_g(const DecodeParams& p, const TcRanges& ranges, int grid, cudaStream_t stream,
+                     int dev) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if ((int)g_attr.size() <= dev) g_attr.resize(dev + 1, 0);
@@ -1198,7 +1217,7 @@ cudaError_t launch_g(const DecodeParams& p, int grid, cudaStream_t stream, int d
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G, E>, p);
+    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G, E>, p, ranges);
 }
 
 }  // namespace
@@ -1208,15 +1227,16 @@ cudaError_t set_decode_wait_limit(uint64_t limit_ns) {
     return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
 }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_decode_tc(const DecodeParams& p, const TcRanges& ranges, int grid,
+                             cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     // slots are held as int32 in the kernel's shared slot lists
     if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
     const bool ext = p.blocks != nullptr;
-    if (p.group_heads == 32) return ext ? launch_g<32, true>(p, grid, stream, dev) : launch_g<32, false>(p, grid, stream, dev);
-    if (p.group_heads == 16) return ext ? launch_g<16, true>(p, grid, stream, dev) : launch_g<16, false>(p, grid, stream, dev);
+    if (p.group_heads == 32) return ext ? launch_g<32, true>(p, ranges, grid, stream, dev) : launch_g<32, false>(p, ranges, grid, stream, dev);
+    if (p.group_heads == 16) return ext ? launch_g<16, true>(p, ranges, grid, stream, dev) : launch_g<16, false>(p, ranges, grid, stream, dev);
     return cudaErrorInvalidValue;
 }
 

@@ -6,6 +6,7 @@
 // The schedule balances work by tokens, not by requests: with contexts drawn
 // from [1024, 8192] a per-request split leaves SMs idle, so the tile list of
 // all requests is cut into equal contiguous ranges (one per CTA).
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -470,6 +471,20 @@ mla_status_t install(mla_plan_t* plan, Schedule&& s, size_t* workspace_bytes, vo
         return MLA_ERR_CUDA;
     }
     p->sched = std::move(s);
+    // the tcgen05 kernel's token ranges as a launch parameter: each range's
+    // segments and its first segment's t0, t1 and page-table offset
+    {
+        const Schedule& sc = p->sched;
+        mla::TcRanges& r = p->ranges;
+        r.n = sc.kernel == mla::DecodeKernel::kTc ? std::min(sc.num_ctas, mla::kMaxTcRanges) : 0;
+        for (int32_t c = 0; c < r.n; ++c) {
+            const int32_t lo = sc.cta_ptr[c], hi = sc.cta_ptr[c + 1];
+            r.seg[c] = lo;
+            r.seg[c + 1] = hi;
+            r.first[c] = lo < hi ? make_int4(sc.segs[4 * lo + 1], sc.segs[4 * lo + 2], sc.seg_pages[lo], 0)
+                                 : make_int4(0, 0, 0, 0);
+        }
+    }
     *workspace_bytes = p->sched.workspace_bytes;
     *plan = p;
     return MLA_OK;

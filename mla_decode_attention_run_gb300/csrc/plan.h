@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "../../include/mla_decode.h"
+#include "decode_params.h"
 
 namespace mla {
 
@@ -99,4 +100,5 @@ struct mla_plan {
     size_t pinned_cap = 0;
     cudaEvent_t upload_done = nullptr;
     size_t off_cta = 0, off_segs = 0, off_merge = 0, off_blocks = 0, off_seg_pages = 0;   // in dev_meta
+    mla::TcRanges ranges;             // tcgen05 path: the token ranges, passed with each launch
 };
