@@ -14,7 +14,7 @@ import workloads as W
 HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mla_decode.h")
 # [q1;q2] as 2 x 16 rows of 576 E4M3 bytes, then 16 fp32 score multipliers and
 # 16 int32 causal limits
-QIMAGE_BYTES = 2 * 16 * 576 + 16 * 8
+QIMAGE_BYTES = 3 * 16 * 576 + 16 * 12      # [q1;q2;q3] rows + two multipliers and a limit per row
 SEGMENT_COST = 2          # tiles' worth of CTA time the tcgen05 schedule charges per segment
 
 

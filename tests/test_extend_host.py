@@ -10,7 +10,7 @@ import pytest
 
 import mla_decode_attention_run_gb300 as M
 
-QIMAGE_BYTES = 2 * 16 * 576 + 16 * 8
+QIMAGE_BYTES = 3 * 16 * 576 + 16 * 12      # [q1;q2;q3] rows + two multipliers and a limit per row
 TILE = 64
 
 
