@@ -54,6 +54,7 @@ struct Schedule {
     std::vector<int32_t> seg_pages;  // per segment: its request's first page-table entry
                                      // (kv_indptr[request]), so the kernel need not look it up
     int32_t part_rows = 0;           // rows per partial slot: H (decode), group_heads (extend)
+    int32_t max_merge_parts = 0;     // the most partials one merge entry folds
     int32_t n_partials = 0;
     // extend: the query rows (new token x head, row = token * H + head) of
     // each request cut into blocks of group_heads rows; 4 ints per block:
@@ -69,6 +70,11 @@ struct Schedule {
 
     int32_t n_segs() const { return static_cast<int32_t>(segs.size() / 4); }
     int32_t n_merge() const { return static_cast<int32_t>(merge.size() / 4); }
+    void count_merge_parts() {
+        max_merge_parts = 0;
+        for (size_t e = 0; e + 3 < merge.size(); e += 4)
+            max_merge_parts = merge[e + 2] > max_merge_parts ? merge[e + 2] : max_merge_parts;
+    }
     int32_t n_blocks() const { return static_cast<int32_t>(blocks.size() / 4); }
 };
 

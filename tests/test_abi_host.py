@@ -130,6 +130,22 @@ def test_schedule_ragged_and_empty_requests():
     _check_schedule(segs, info, lens, 4, num_sms=5)
 
 
+def test_schedule_many_short_requests_over_sm_counts():
+    """Several one-tile requests and few CTAs: every request costs a segment,
+    so the search for the cost cap must start from a cap that one CTA can
+    always meet (every request whole, one segment each)."""
+    g = np.random.default_rng(5)
+    cases = [np.array([1, 2, 3]), np.array([64, 1, 1, 1, 65]), np.full(9, 5),
+             g.integers(0, 200, 17), g.integers(1, 70, 40)]
+    for lens in cases:
+        for heads in (16, 64):
+            for num_sms in (1, 2, 3, 4, 7, 19, 152):
+                segs, info = M.mla_decode_schedule(_indptr(lens, 1), lens, len(lens), heads, 1,
+                                                   num_sms=num_sms)
+                assert info["num_ctas"] >= 1
+                _check_schedule(segs, info, lens, heads, num_sms=num_sms)
+
+
 def test_schedule_picks_the_tensor_core_kernel_for_fp8_pools():
     lens = np.array([1000, 3000])
     _, fp8_16 = M.mla_decode_schedule(_indptr(lens, 1), lens, 2, 16, 1, M.MLA_KV_FP8_E4M3)
