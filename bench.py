@@ -437,9 +437,11 @@ def measure_step(torch, M, args, B, pools, k_scales, stream, dist, world, local,
     # The step's inputs go up and its outputs come back a chunk of layers at a
     # time on two copy streams, so that each chunk's copies overlap the
     # neighbouring chunks' store + decode (every byte still crosses within the
-    # timed step).
-    # small chunks at both ends (the first upload and the last download are
-    # not hidden), large ones in the middle
+    # timed step); small chunks at both ends (the first upload and the last
+    # download are not hidden), large ones in the middle.  The copies, the
+    # stores and the decode calls of a step are captured together as one CUDA
+    # graph on three streams joined by events, so that a step costs the host
+    # one plan and one replay.
     ramp = [2, 4, 8]
     sizes = ramp + [max(1, (L - 2 * sum(ramp)) // 3)] * 3 + ramp[::-1]
     if sum(sizes) > L or L < 2 * sum(ramp) + 3:
@@ -449,46 +451,42 @@ def measure_step(torch, M, args, B, pools, k_scales, stream, dist, world, local,
     for z in sizes:
         bounds.append(bounds[-1] + z)
     spans = list(zip(bounds[:-1], bounds[1:]))
-    n_chunks = len(spans)
-    g_chunks = [capture(lambda s, a=a, b=b: [(store(l, s), decode(l, s)) for l in range(a, b)])
-                for a, b in spans]
     up_s, down_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_prev = torch.cuda.Event()
+    ev_start, ev_out = torch.cuda.Event(), torch.cuda.Event()
     ev_in = [torch.cuda.Event() for _ in spans]
     ev_done = [torch.cuda.Event() for _ in spans]
-    ev_out = torch.cuda.Event()
 
-    def upload(c):
-        a, b = spans[c]
-        with torch.cuda.stream(up_s):
-            q[a:b].copy_(h_q[a:b], non_blocking=True)
-            new_ckv[a:b].copy_(h_ckv[a:b], non_blocking=True)
-            new_kpe[a:b].copy_(h_kpe[a:b], non_blocking=True)
-            ev_in[c].record(up_s)
-
-    def e2e_step():
-        # the previous step has read its inputs before they are overwritten
-        ev_prev.record(stream)
-        up_s.wait_event(ev_prev)
-        down_s.wait_event(ev_prev)
+    def e2e_body(s):
+        ev_start.record(s)
+        up_s.wait_event(ev_start)
+        down_s.wait_event(ev_start)
         with torch.cuda.stream(up_s):
             for d, h in zip((indptr_d, idx_d, lens_d), h_pt):
                 d.copy_(h, non_blocking=True)
             slots_d.copy_(h_slots, non_blocking=True)
-        upload(0)
-        plan_step()
+            for c, (a, b) in enumerate(spans):
+                q[a:b].copy_(h_q[a:b], non_blocking=True)
+                new_ckv[a:b].copy_(h_ckv[a:b], non_blocking=True)
+                new_kpe[a:b].copy_(h_kpe[a:b], non_blocking=True)
+                ev_in[c].record(up_s)
         for c, (a, b) in enumerate(spans):
-            if c + 1 < len(spans):
-                upload(c + 1)
-            stream.wait_event(ev_in[c])
-            g_chunks[c].replay()
-            ev_done[c].record(stream)
+            s.wait_event(ev_in[c])
+            for l in range(a, b):
+                store(l, s)
+                decode(l, s)
+            ev_done[c].record(s)
             down_s.wait_event(ev_done[c])
             with torch.cuda.stream(down_s):
                 h_out[a:b].copy_(out[a:b], non_blocking=True)
                 h_lse[a:b].copy_(lse[a:b], non_blocking=True)
         ev_out.record(down_s)
-        stream.wait_event(ev_out)
+        s.wait_event(ev_out)
+
+    g_e2e = capture(e2e_body)
+
+    def e2e_step():
+        plan_step()
+        g_e2e.replay()
 
     with torch.cuda.stream(stream):
         for _ in range(2):
@@ -502,7 +500,8 @@ def measure_step(torch, M, args, B, pools, k_scales, stream, dist, world, local,
                      "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                      "per": "layer-call incl. store and host copies",
                      "overlap": f"inputs up and outputs down per chunk of layers {sizes} on two copy "
-                                "streams, overlapping compute"}
+                                "streams, overlapping compute; copies, stores and decode calls of a step "
+                                "in one CUDA graph, the plan on the host before it"}
 
     # ---- the two baselines the pages describe, per decode step
     if not args.no_baselines:
@@ -521,7 +520,7 @@ def measure_step(torch, M, args, B, pools, k_scales, stream, dist, world, local,
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline_from_device(pools[0], q[0], indptr, idx, lens,
                                                           k_scales[0], B)
-    del g_step, g_decode
+    del g_step, g_decode, g_e2e
     M.mla_decode_plan_destroy(plan)
     return result
 
