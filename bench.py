@@ -578,7 +578,8 @@ def measure_configs(torch, M, dev, stream, names=("single", "large_head")):
         nbytes = A.decode_call_bytes(w.seq_lens, H, ps)
         flops = A.decode_call_flops(w.seq_lens, H)
         r = {"batch": B, "heads": H, "page_size": ps, "tokens": int(w.seq_lens.sum()),
-             "kernel": "tcgen05" if kernel == 1 else "mma.sync", "us_per_call": round(us, 3),
+             "kernel": "tcgen05" if kernel == 1 else "mma.sync",
+             "token_ranges": M.mla_decode_plan_info(plan)["num_ctas"], "us_per_call": round(us, 3),
              "achieved_gbs": round(nbytes / us / 1e3, 1), "hbm_frac": round(nbytes / us / 1e3 / peak, 4),
              "tflops": round(flops / us / 1e6, 2),
              "l2": "the whole call fits in L2 (latency-bound)" if nbytes < 64e6 else "inputs larger than L2"}

@@ -209,7 +209,10 @@ __global__ void __launch_bounds__(kPThreads, 1) kv_proj_store_kernel(const ProjP
     if (warp >= 2) {
         const int q = warp & 3;
         const int row = M == 128 ? q * 32 + lane : (lane < 16 ? q * 16 + lane : M);
-        const bool ok = mbar_wait(&bars[DONE], 0, abort, p.flags);
+        // a drain: the MMA thread commits DONE on every path, and TMEM is read
+        // (and later released) only once its MMAs have completed
+        volatile int never = 0;
+        const bool ok = mbar_wait(&bars[DONE], 0, &never, p.flags, 1000000000ull) && *abort == 0;
         fence_after_sync();
         const int prow = row < rows ? row : 0;            // address only used when row < rows
         const uint32_t dst = cluster_map(smem_u32(red + (rank * rpo + prow / split) * S::kRedStride),

@@ -209,6 +209,7 @@ def test_decode_large_head_full_size_sampled():
     (32, 2, [300, 77]),
     (48, 1, [513]),
     (64, 1, [2000, 5, 700, 64]),                   # 32-head CTAs in two head groups
+    (96, 8, [777, 64, 1, 130]),                    # clusters of three sharing tiles
     (128, 64, [1000, 64, 3]),
 ])
 def test_decode_edge_shapes(heads, ps, lens):
@@ -222,8 +223,12 @@ def test_decode_edge_shapes(heads, ps, lens):
     check_attention(out, lse, o_ref, lse_ref, f"H={heads} ps={ps} lens={lens}")
 
 
-def test_decode_strided_q_and_separate_pools():
-    w = W.make_workload("concurrency", batch=3, lens=[200, 1, 777], num_slots=3000, seed=5)
+@pytest.mark.parametrize("heads", [16, 64, 128])
+def test_decode_strided_q_and_separate_pools(heads):
+    """Padded c_kv and k_pe pools of their own (H = 64, 128: the head groups
+    of a token range gather through two row maps and share tiles)."""
+    w = W.make_workload("concurrency", batch=3, heads=heads, lens=[200, 1, 777], num_slots=3000,
+                        seed=5)
     pool = oracle_pool(w)
     ckv0 = np.zeros((w.num_slots, 528), np.uint8)
     kpe0 = np.zeros((w.num_slots, 96), np.uint8)
@@ -237,7 +242,7 @@ def test_decode_strided_q_and_separate_pools():
     assert M.mla_get_last_error() == 0
     o_ref, lse_ref = oracle.decode_fp8(w.q_bf16, pool[:, :512], pool[:, 512:], w.kv_indptr,
                                        w.kv_indices, w.seq_lens, 1, w.k_scale, w.softmax_scale)
-    check_attention(out, lse, o_ref, lse_ref, "strided")
+    check_attention(out, lse, o_ref, lse_ref, f"strided H={heads}")
 
 
 def test_decode_is_deterministic():
