@@ -53,12 +53,18 @@ struct TcRanges {
 };
 
 // The 32-head decode CTAs of one token range (H = 64, 96, 128: two to four
-// head groups) run as one thread-block cluster and share each tile: every
-// CTA gathers a share of the tile's rows with TMA and multicasts them to all
-// of the cluster, so a row leaves L2 once instead of once per head group.
+// head groups) run as thread-block clusters that share each tile: every CTA
+// gathers a share of the tile's rows with TMA and multicasts them to all of
+// its cluster, so a row leaves L2 once per cluster instead of once per head
+// group.  Clusters are pairs of head groups where the count is even (H = 64,
+// 128): a GPC of GB300 holds 9 or 10 of them, so every SM takes a CTA, where
+// clusters of four leave two to four SMs of a GPC idle (measured: 2.32 ms
+// against 2.20 without sharing for the 128-head call, whose tiles are bound
+// by the MMA and softmax chain rather than by the gather).
 inline bool tc_shares_tiles(int group_heads, int head_groups) {
     return group_heads == 32 && head_groups >= 2 && head_groups <= 4;
 }
+inline int tc_cluster_size(int head_groups) { return head_groups % 2 == 0 ? 2 : head_groups; }
 
 // Clusters of `size` 32-head decode CTAs that the current device holds at
 // once (0 on error); the plan keeps its token ranges within it.

@@ -37,9 +37,10 @@
 // softmax warps rescale it in place before the next PV may add to it.
 //
 // A CTA serves G = 16 or 32 heads of its token range (32 when H is a multiple
-// of 32); more heads run as more CTAs (grid.y = head group).  The groups of a
-// token range start together, so their repeated reads of the same rows
-// mostly hit L2.
+// of 32); more heads run as more CTAs (grid.y = head group).  The 32-head
+// groups of a token range (H = 64, 96, 128) run as thread-block clusters of
+// two (three for H = 96) that share every tile: each CTA gathers a share of
+// the rows with TMA tile::gather4 and multicasts it to the whole cluster.
 //
 // Extend (several new tokens per request, causal) is the same kernel built
 // with E = true: a CTA then serves a block of G query rows (token x head) of
@@ -1376,9 +1377,9 @@ cudaError_t launch_g(const DecodeParams& p, const TcRanges& ranges, const TcMaps
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;    // the head groups of a token range
+    attr[1].id = cudaLaunchAttributeClusterDimension;    // head groups of a token range
     attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = p.head_groups;
+    attr[1].val.clusterDim.y = tc_cluster_size(p.head_groups);
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = kMc ? 2 : 1;

@@ -531,12 +531,13 @@ extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indp
     if (st != MLA_OK) return st;
     int sms = mla::device_sm_count();
     if (sms <= 0) return MLA_ERR_CUDA;
-    // head groups that share tiles run as clusters: no more token ranges than
-    // the device holds clusters at once (a second wave would double the call)
+    // head groups that share tiles run as clusters: no more CTAs than the
+    // device holds in clusters at once (a second wave would double the call)
     if (kv_dtype == MLA_KV_FP8_E4M3 && num_heads % 32 == 0 &&
         mla::tc_shares_tiles(32, num_heads / 32)) {
-        const int clusters = mla::tc_cluster_capacity(num_heads / 32);
-        if (clusters > 0 && clusters * (num_heads / 32) < sms) sms = clusters * (num_heads / 32);
+        const int size = mla::tc_cluster_size(num_heads / 32);
+        const int clusters = mla::tc_cluster_capacity(size);
+        if (clusters > 0 && clusters * size < sms) sms = clusters * size;
     }
     Schedule s;
     st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads, page_size,
