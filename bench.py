@@ -525,7 +525,7 @@ def measure_step(torch, M, args, B, pools, k_scales, stream, dist, world, local,
     return result
 
 
-def measure_configs(torch, M, dev, stream, names=("single", "large_head")):
+def measure_configs(torch, M, dev, stream, names=("single", "large_head"), batch=None):
     """The single-stream (1 x 4,096 tokens) and 128-head (128 x 32,768 tokens,
     page size 64, 2.4 GB pool) decode calls, each timed as a CUDA graph of
     back-to-back calls on pools of quantized N(0, 0.5) latents.  The
@@ -541,7 +541,8 @@ def measure_configs(torch, M, dev, stream, names=("single", "large_head")):
     for name, reps in (("single", 50), ("large_head", 4)):
         if name not in names:
             continue
-        w = W.make_workload(name, latent_requests=[])
+        # batch: fewer requests of the same shape (a smaller case for profilers)
+        w = W.make_workload(name, latent_requests=[], **({"batch": batch} if batch else {}))
         B, H, ps = w.batch, w.heads, w.page_size
         pool = torch.empty((w.num_slots, W.D_ALL), dtype=torch.uint8, device=dev)
         k_scale = latent_pool_(torch, pool, seed=11)
@@ -991,6 +992,9 @@ def main(argv=None):
                          "print its JSON (a diagnostic)")
     ap.add_argument("--config", choices=["single", "large_head"],
                     help="time only that decode configuration and print its JSON (a diagnostic)")
+    ap.add_argument("--config-batch", type=int, default=None,
+                    help="with --config: that many requests of the configuration's shape (a smaller "
+                         "case for profilers)")
     ap.add_argument("--pools", type=int, default=8,
                     help="pools the extend timing rotates over (--extend-only)")
     args = ap.parse_args(argv)
@@ -1015,7 +1019,8 @@ def main(argv=None):
         import mla_decode_attention_run_gb300 as M
         torch.cuda.set_device(local)
         stream = torch.cuda.Stream()
-        res = measure_configs(torch, M, torch.device("cuda", local), stream, names=(args.config,))
+        res = measure_configs(torch, M, torch.device("cuda", local), stream, names=(args.config,),
+                              batch=args.config_batch)
         if rank == 0:
             print(json.dumps({"configs": res}), flush=True)
         return

@@ -1,7 +1,6 @@
 // Launch parameters shared by the decode kernels (decode.cu, decode_tc.cu).
 #pragma once
 
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -51,24 +50,6 @@ struct TcRanges {
     int32_t seg[kMaxTcRanges + 1];      // range c: segments [seg[c], seg[c + 1])
     int4 first[kMaxTcRanges];           // range c's first segment: t0, t1, page-table offset, 0
 };
-
-// The 32-head decode CTAs of one token range (H = 64, 96, 128: two to four
-// head groups) run as thread-block clusters that share each tile: every CTA
-// gathers a share of the tile's rows with TMA and multicasts them to all of
-// its cluster, so a row leaves L2 once per cluster instead of once per head
-// group.  Clusters are pairs of head groups where the count is even (H = 64,
-// 128): a GPC of GB300 holds 9 or 10 of them, so every SM takes a CTA, where
-// clusters of four leave two to four SMs of a GPC idle (measured: 2.32 ms
-// against 2.20 without sharing for the 128-head call, whose tiles are bound
-// by the MMA and softmax chain rather than by the gather).
-inline bool tc_shares_tiles(int group_heads, int head_groups) {
-    return group_heads == 32 && head_groups >= 2 && head_groups <= 4;
-}
-inline int tc_cluster_size(int head_groups) { return head_groups % 2 == 0 ? 2 : head_groups; }
-
-// Clusters of `size` 32-head decode CTAs that the current device holds at
-// once (0 on error); the plan keeps its token ranges within it.
-int tc_cluster_capacity(int size);
 
 // Launches the q split kernel and then, as its programmatic dependent, the
 // tcgen05 FP8 decode kernel (decode_tc.cu) on `grid` token ranges x

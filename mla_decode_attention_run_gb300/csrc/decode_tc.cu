@@ -37,10 +37,9 @@
 // softmax warps rescale it in place before the next PV may add to it.
 //
 // A CTA serves G = 16 or 32 heads of its token range (32 when H is a multiple
-// of 32); more heads run as more CTAs (grid.y = head group).  The 32-head
-// groups of a token range (H = 64, 96, 128) run as thread-block clusters of
-// two (three for H = 96) that share every tile: each CTA gathers a share of
-// the rows with TMA tile::gather4 and multicasts it to the whole cluster.
+// of 32); more heads run as more CTAs (grid.y = head group).  The groups of a
+// token range start together, so their repeated reads of the same rows
+// mostly hit L2.
 //
 // Extend (several new tokens per request, causal) is the same kernel built
 // with E = true: a CTA then serves a block of G query rows (token x head) of
@@ -74,7 +73,6 @@
 //              channel).
 // Every mbarrier wait is bounded; on a timeout the CTA sets
 // MLA_FLAG_WAIT_TIMEOUT, drains its MMAs and copies, frees TMEM and exits.
-#include <cstring>
 #include <mutex>
 #include <vector>
 
@@ -181,14 +179,6 @@ enum : int {
 };
 static_assert(NUM_BARS * 8 <= 512, "barrier space");
 
-// Row-gather tensor maps over the pool (shared tiles only): c_kv as
-// [num_slots][512] E4M3 with boxes of 128 channels x 1 row (128-byte
-// swizzle), k_pe as [num_slots][64] with boxes of one 64-byte row (64-byte
-// swizzle): the stage layout the fill warps' cp.async writes.
-struct TcMaps {
-    CUtensorMap ckv, kpe;
-};
-
 // b: the request, or (extend) the query block; req: the request whose pages
 // and context the segment reads
 struct Seg {
@@ -243,16 +233,9 @@ constexpr int32_t kNoRow = INT32_MIN;
 // A wait made by every lane of a warp that then acts together (shuffles,
 // warp barriers): the warp goes on only if every lane's wait succeeded, so
 // that after an abort no lane leaves the loop while the others stay in it.
-// kLive: a phase seen complete after the abort fails too (mbar_wait_live).
-template <bool kLive>
-__device__ __forceinline__ bool wait_as(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags) {
-    return kLive ? mbar_wait_live(bar, parity, abort, flags) : mbar_wait(bar, parity, abort, flags);
-}
-
-template <bool kLive = false>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* flags) {
-    return __all_sync(0xffffffffu, wait_as<kLive>(bar, parity, abort, flags));
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, flags));
 }
 
 // Cursor over the tiles of a CTA's segments, with the raw page entries of
@@ -357,16 +340,13 @@ __device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage
     }
 }
 
-// cur: started by the caller (its first page entries already requested).
-// With shared tiles (a cluster of ncta CTAs) this CTA prefetches only the
-// rows it gathers: 4-row groups g with g % ncta == rank.
+// cur: started by the caller (its first page entries already requested)
 template <bool E>
 __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                          TileCursor<E>& cur, int lane, uint32_t rank, uint32_t ncta) {
+                          TileCursor<E>& cur, int lane) {
     int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
     // one prefetch sweep per row when k_pe follows c_kv in the same row
     const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
-    const bool mine = static_cast<uint32_t>(lane >> 1) % ncta == rank;   // rows 2 lane, 2 lane + 1
     // publishes every tile as soon as its ring entry is free (the ring bounds
     // how far ahead of the softmax warps the prefetches run)
     for (int n = 0; cur.valid(); ++n) {
@@ -378,7 +358,7 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
         if (!warp_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            if (sl[q] < 0 || !mine) continue;
+            if (sl[q] < 0) continue;
             const uint8_t* row = p.ckv + int64_t(sl[q]) * p.ckv_stride;
             if (joint) {
                 prefetch_row_l2<kDQk>(row);
@@ -415,79 +395,10 @@ __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     cp_async_wait<0>();
 }
 
-// Shared tiles: warp 0 of each CTA of the cluster gathers its 4-row groups
-// (g % ncta == rank) of every tile with TMA tile::gather4 and multicasts them
-// to the same stage of every CTA; each CTA's KV_FULL expects the whole tile,
-// and a stage is refilled once every CTA's PV has released it (KV_EMPTY
-// counts one multicast commit per CTA).  Lane l issues boxes l and l + 32
-// of the CTA's (group, box) list: boxes 0-3 are the group's c_kv channel
-// blocks (512 B), box 4 its k_pe rows (256 B).
-template <bool E>
-__device__ void fill_tma(const DecodeParams& p, const TcMaps& maps, uint8_t* base, uint64_t* bars,
-                         volatile int* abort, int seg_lo, int seg_hi, int lane, uint32_t rank,
-                         uint32_t ncta) {
-    const int32_t* ring = reinterpret_cast<const int32_t*>(base + kOffRing);
-    const uint32_t sbase = smem_u32(base);
-    const uint16_t mask = static_cast<uint16_t>((1u << ncta) - 1);
-    const int groups = static_cast<int>((kTT / 4 - rank + ncta - 1) / ncta);
-    const int total = count_tiles<E>(p, seg_lo, seg_hi);
-    const int32_t oob = static_cast<int32_t>(p.num_slots);     // reads as zeros
-    for (int i = 0; i < total; ++i) {
-        const int slot = i % kStages;
-        const uint32_t u = static_cast<uint32_t>(i / kStages);
-        const int e = i % kRing;
-        if (!warp_wait<true>(&bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, abort, p.flags)) break;
-        int4 rows[2];
-        int box[2], g[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int item = lane + 32 * q;
-            g[q] = static_cast<int>(rank + ncta * static_cast<uint32_t>(item / 5));
-            box[q] = item % 5;
-            rows[q] = make_int4(oob, oob, oob, oob);
-            if (item < 5 * groups) {
-                rows[q] = *reinterpret_cast<const int4*>(ring + e * kTT + 4 * g[q]);
-                rows[q].x = rows[q].x < 0 ? oob : rows[q].x;
-                rows[q].y = rows[q].y < 0 ? oob : rows[q].y;
-                rows[q].z = rows[q].z < 0 ? oob : rows[q].z;
-                rows[q].w = rows[q].w < 0 ? oob : rows[q].w;
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[SL_EMPTY + e]);
-        if (!warp_wait<true>(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
-        // (a successful wait above also means this CTA had not aborted: the
-        // stage's previous phase is complete, so the arrival below opens the
-        // next one)
-        if (lane == 0) mbar_arrive_expect_tx(&bars[KV_FULL + slot], kStage);
-        __syncwarp();
-        const uint32_t stage = sbase + kOffStage + slot * kStage;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            if (lane + 32 * q >= 5 * groups) continue;
-            if (box[q] < 4)
-                tma_gather4_mc(stage + box[q] * kBlk + g[q] * 512, &maps.ckv, box[q] * 128, rows[q],
-                               &bars[KV_FULL + slot], mask);
-            else
-                tma_gather4_mc(stage + 4 * kBlk + g[q] * 256, &maps.kpe, 0, rows[q], &bars[KV_FULL + slot],
-                               mask);
-        }
-    }
-    // After an abort, copies this CTA issued may still be on their way to
-    // the cluster's shared memory: they land within microseconds, so the
-    // CTA waits 200 us before it meets the cluster at the exit barrier.
-    if (*abort) {
-        const uint64_t t0 = global_ns();
-        while (global_ns() - t0 < 200000ull) {
-        }
-    }
-}
-
 // ------------------------------------------------------------- MMA issuer
 
 struct MmaCtx {
     uint32_t sbase, tmem, idesc_qk, idesc_pv;
-    uint16_t cta_mask;                  // shared tiles: every CTA of the cluster
     uint64_t* bars;
     volatile int* abort;
     uint32_t* flags;
@@ -527,7 +438,7 @@ __device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
 }
 
 // PV of tile j into O buffer `ob`; the segment's first tile overwrites it.
-template <int G, bool kMc>
+template <int G>
 __device__ __forceinline__ void issue_pv(const MmaCtx& c, int j, int ob, bool first) {
     using S = Shape<G>;
     const int kv = j % kStages;
@@ -545,10 +456,7 @@ __device__ __forceinline__ void issue_pv(const MmaCtx& c, int j, int ob, bool fi
                      c.idesc_pv, ks > 0 || !first);
     }
     mma_commit(&c.bars[PV_DONE + (j & 1)]);
-    // the stage may be refilled (shared tiles: once every CTA of the cluster
-    // has released it)
-    if constexpr (kMc) mma_commit_mc(&c.bars[KV_EMPTY + kv], c.cta_mask);
-    else mma_commit(&c.bars[KV_EMPTY + kv]);
+    mma_commit(&c.bars[KV_EMPTY + kv]);       // the stage may be refilled
 }
 
 // Position in the CTA's tile sequence: segment ordinal k and tile it of it.
@@ -611,7 +519,7 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
     mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
 }
 
-template <int G, bool E, bool kMc>
+template <int G, bool E>
 __device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
     using S = Shape<G>;
     const int total = count_tiles<E>(p, seg_lo, seg_hi);
@@ -619,15 +527,15 @@ __device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, in
     wp.init(p, seg_lo, seg_hi);
     for (int pv = 0; pv < total; ++pv) {
         const int ob = wp.k % S::kOBufs;
-        if (!wait_as<kMc>(&c.bars[P_FULL + (pv & 1)], (static_cast<uint32_t>(pv) >> 1) & 1, c.abort, c.flags)) break;
+        if (!mbar_wait(&c.bars[P_FULL + (pv & 1)], (static_cast<uint32_t>(pv) >> 1) & 1, c.abort, c.flags)) break;
         // a segment's first PV overwrites its O buffer: the segment that used
         // it before has been read out
         if (wp.it == 0 &&
-            !wait_as<kMc>(&c.bars[O_FREE + ob], (static_cast<uint32_t>(wp.k / S::kOBufs) & 1) ^ 1, c.abort, c.flags))
+            !mbar_wait(&c.bars[O_FREE + ob], (static_cast<uint32_t>(wp.k / S::kOBufs) & 1) ^ 1, c.abort, c.flags))
             break;
         fence_after_sync();
         fence_proxy_async_smem();
-        issue_pv<G, kMc>(c, pv, ob, wp.it == 0);
+        issue_pv<G>(c, pv, ob, wp.it == 0);
         wp.advance(p);
     }
     mma_commit(&c.bars[DONE]);
@@ -1173,13 +1081,10 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
 // programmatic launch places decode CTAs while the split still runs (at 160
 // registers they waited for the split to drain; measured on GB300).  At
 // G = 32 the CTA runs 512 threads (two softmax warpgroups) at 128 registers.
-template <int G, bool E, bool kMc>
+template <int G, bool E>
 __global__ void __maxnreg__(G == 16 ? 152 : 128)
-    mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TcRanges ranges,
-                         const __grid_constant__ TcMaps maps) {
+    mla_decode_tc_kernel(const DecodeParams p, const __grid_constant__ TcRanges ranges) {
     using S = Shape<G>;
-    // kMc: the CTA is one of a cluster that shares every tile (its rank and size)
-    const uint32_t rank = kMc ? cluster_ctarank() : 0, ncta = kMc ? cluster_nctarank() : 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBar);
@@ -1198,12 +1103,10 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
         // PV_DONE, Q_FULL: one commit or bulk-copy arrival; S_FREE, P_FULL,
         // O_FREE: every softmax thread; Q_FREE: those and the QK commit; DONE:
         // both MMA threads; SL_EMPTY: the fill warps and the softmax warps
-        // (shared tiles: KV_FULL one arrive.expect_tx, KV_EMPTY one commit per
-        // CTA of the cluster, SL_EMPTY warp 0 of the fill warps)
         constexpr uint32_t kSm = 128 * S::kWgs;
         for (int b = 0; b < kStages; ++b) {
-            mbar_init(&bars[KV_FULL + b], kMc ? 1 : 32 * kFillWarps);
-            mbar_init(&bars[KV_EMPTY + b], kMc ? ncta : 1);
+            mbar_init(&bars[KV_FULL + b], 32 * kFillWarps);
+            mbar_init(&bars[KV_EMPTY + b], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&bars[S_FULL + b], 1);
@@ -1217,33 +1120,22 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
         mbar_init(&bars[DONE], 2);
         for (int e = 0; e < kRing; ++e) {
             mbar_init(&bars[SL_FULL + e], 1);
-            mbar_init(&bars[SL_EMPTY + e], (kMc ? 1 : kFillWarps) + 4 * S::kWgs);
+            mbar_init(&bars[SL_EMPTY + e], kFillWarps + 4 * S::kWgs);
         }
         *abort = 0;
         mbar_fence_init();
     }
     if (warp == kWarpMma) tmem_alloc(tmem_slot, kTmemCols);
     fence_before_sync();
-    // shared tiles: every CTA's barriers are initialised before any copy or
-    // commit of the cluster reaches them
-    if constexpr (kMc) {
-        __syncwarp();                             // barrier.cluster is warp-aligned
-        cluster_sync();
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
     fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == S::kWarpSched) {
-        scheduler<E>(p, base, bars, abort, cur, lane, rank, ncta);
+        scheduler<E>(p, base, bars, abort, cur, lane);
     } else if (warp < kFillWarps) {
-        if constexpr (kMc) {
-            if (warp == 0) fill_tma<E>(p, maps, base, bars, abort, seg_lo, seg_hi, lane, rank, ncta);
-        } else {
-            fill_warp<E>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
-        }
+        fill_warp<E>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
     } else if (warp == kWarpMma || warp == S::kWarpPv) {
         if (lane == 0) {
             MmaCtx c;
@@ -1254,9 +1146,8 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
             c.bars = bars;
             c.abort = abort;
             c.flags = p.flags;
-            c.cta_mask = static_cast<uint16_t>((1u << ncta) - 1);
             if (warp == kWarpMma) qk_issuer<G, E>(p, c, seg_lo, seg_hi);
-            else pv_issuer<G, E, kMc>(p, c, seg_lo, seg_hi);
+            else pv_issuer<G, E>(p, c, seg_lo, seg_hi);
         }
         __syncwarp();
     } else if (warp == kWarpQ) {
@@ -1279,14 +1170,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
         softmax_wg<G, E>(p, w, seg_lo, seg_hi, head0);
     }
     fence_before_sync();
-    // shared tiles: no CTA leaves while the cluster's copies and commits may
-    // still reach its shared memory
-    if constexpr (kMc) {
-        __syncwarp();                             // barrier.cluster is warp-aligned
-        cluster_sync();
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
     fence_after_sync();
     if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
     // this CTA's work is done: the merge kernel may be launched once every
@@ -1295,78 +1179,32 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
 }
 
 std::mutex g_mu;
-std::vector<char> g_attr;     // per device: bit (G / 16 - 1) + 2 E + 4 kMc: max dynamic smem set
+std::vector<char> g_attr;     // per device: bit (G / 16 - 1) + 2 E: max dynamic smem set
 
-template <int G, bool E, bool kMc>
-cudaError_t prepare(int dev) {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if ((int)g_attr.size() <= dev) g_attr.resize(dev + 1, 0);
-    const char bit = static_cast<char>(1 << ((G / 16 - 1) + 2 * E + 4 * kMc));
-    if (g_attr[dev] & bit) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<G, E, kMc>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    // the split uses no shared memory; an SM configured for it with a
-    // small carveout could not take a decode CTA until it drained
-    const cudaError_t e2 = cudaFuncSetAttribute(mla_q_split_kernel<G>,
-                                                cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                cudaSharedmemCarveoutMaxShared);
-    if (e2 != cudaSuccess) return e2;
-    g_attr[dev] |= bit;
-    return cudaSuccess;
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            f = nullptr;
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
-
-// Row-gather map over `rows` rows of `width` E4M3 channels, `stride` bytes
-// apart, boxes of `width` x 1.  False when the driver refuses it (a base
-// or stride that is not a multiple of 16 bytes).
-bool encode_rows(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t stride,
-                 CUtensorMapSwizzle swz) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn || rows == 0) return false;
-    const cuuint64_t dims[2] = {width, rows};
-    const cuuint64_t strides[1] = {stride};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(width), 1};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-bool encode_maps(const DecodeParams& p, TcMaps* maps) {
-    // a c_kv box is 128 channels: the map covers channels 0..511 of each row
-    return encode_rows(&maps->ckv, p.ckv, kDCkv, static_cast<uint64_t>(p.num_slots),
-                       static_cast<uint64_t>(p.ckv_stride), CU_TENSOR_MAP_SWIZZLE_128B) &&
-           encode_rows(&maps->kpe, p.kpe, kDKpe, static_cast<uint64_t>(p.num_slots),
-                       static_cast<uint64_t>(p.kpe_stride), CU_TENSOR_MAP_SWIZZLE_64B);
-}
-
-template <int G, bool E, bool kMc>
-cudaError_t launch_g(const DecodeParams& p, const TcRanges& ranges, const TcMaps& maps, int grid,
-                     cudaStream_t stream, int dev) {
-    cudaError_t e = prepare<G, E, kMc>(dev);
-    if (e != cudaSuccess) return e;
+template <int G, bool E>
+cudaError_t launch_g(const DecodeParams& p, const TcRanges& ranges, int grid, cudaStream_t stream,
+                     int dev) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if ((int)g_attr.size() <= dev) g_attr.resize(dev + 1, 0);
+        const char bit = static_cast<char>(1 << ((G / 16 - 1) + 2 * E));
+        if (!(g_attr[dev] & bit)) {
+            const cudaError_t e = cudaFuncSetAttribute(mla_decode_tc_kernel<G, E>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+            if (e != cudaSuccess) return e;
+            // the split uses no shared memory; an SM configured for it with a
+            // small carveout could not take a decode CTA until it drained
+            const cudaError_t e2 = cudaFuncSetAttribute(mla_q_split_kernel<G>,
+                                                        cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                        cudaSharedmemCarveoutMaxShared);
+            if (e2 != cudaSuccess) return e2;
+            g_attr[dev] |= bit;
+        }
+    }
     const int64_t images = E ? p.n_blocks : int64_t(p.batch) * p.head_groups;
     const int split_blocks = static_cast<int>((images * G * 32 + kSplitThreads - 1) / kSplitThreads);
     mla_q_split_kernel<G><<<split_blocks, kSplitThreads, 0, stream>>>(p);
-    e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // the decode kernel starts while the split runs: only its q warp waits
     cudaLaunchConfig_t cfg = {};
@@ -1374,52 +1212,15 @@ cudaError_t launch_g(const DecodeParams& p, const TcRanges& ranges, const TcMaps
     cfg.blockDim = dim3(Shape<G>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;    // head groups of a token range
-    attr[1].val.clusterDim.x = 1;
-    attr[1].val.clusterDim.y = tc_cluster_size(p.head_groups);
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = kMc ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G, E, kMc>, p, ranges, maps);
-}
-
-std::vector<std::vector<int>> g_capacity;   // per device, per cluster size: -1 unknown
-
-}  // namespace
-
-int tc_cluster_capacity(int size) {
-    if (size < 2 || size > 4) return 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if ((int)g_capacity.size() <= dev) g_capacity.resize(dev + 1, std::vector<int>(5, -1));
-        if (g_capacity[dev][size] >= 0) return g_capacity[dev][size];
-    }
-    if (prepare<32, false, true>(dev) != cudaSuccess) return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, size);
-    cfg.blockDim = dim3(Shape<32>::kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 1;
-    attr[0].val.clusterDim.y = size;
-    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_tc_kernel<32, false, true>, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_capacity[dev][size] = n;
-    return n;
+    return cudaLaunchKernelEx(&cfg, mla_decode_tc_kernel<G, E>, p, ranges);
 }
+
+}  // namespace
 
 cudaError_t set_decode_wait_limit(uint64_t limit_ns) {
     const uint64_t v = limit_ns ? limit_ns : kDefaultWaitLimitNs;
@@ -1434,18 +1235,8 @@ cudaError_t launch_decode_tc(const DecodeParams& p, const TcRanges& ranges, int 
     // slots are held as int32 in the kernel's shared slot lists
     if (p.num_slots >= INT32_MAX) return cudaErrorInvalidValue;
     const bool ext = p.blocks != nullptr;
-    TcMaps maps;
-    std::memset(&maps, 0, sizeof(maps));
-    // the head groups of a token range share tiles when the pool's rows can
-    // be gathered by TMA (16-byte aligned base and stride)
-    if (!ext && tc_shares_tiles(p.group_heads, p.head_groups) && encode_maps(p, &maps))
-        return launch_g<32, false, true>(p, ranges, maps, grid, stream, dev);
-    if (p.group_heads == 32)
-        return ext ? launch_g<32, true, false>(p, ranges, maps, grid, stream, dev)
-                   : launch_g<32, false, false>(p, ranges, maps, grid, stream, dev);
-    if (p.group_heads == 16)
-        return ext ? launch_g<16, true, false>(p, ranges, maps, grid, stream, dev)
-                   : launch_g<16, false, false>(p, ranges, maps, grid, stream, dev);
+    if (p.group_heads == 32) return ext ? launch_g<32, true>(p, ranges, grid, stream, dev) : launch_g<32, false>(p, ranges, grid, stream, dev);
+    if (p.group_heads == 16) return ext ? launch_g<16, true>(p, ranges, grid, stream, dev) : launch_g<16, false>(p, ranges, grid, stream, dev);
     return cudaErrorInvalidValue;
 }
 

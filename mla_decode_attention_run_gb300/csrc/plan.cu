@@ -529,16 +529,8 @@ extern "C" mla_status_t mla_decode_plan(mla_plan_t* plan, const int32_t* kv_indp
     mla_status_t st = mla::validate_plan_inputs(kv_indptr_host, seq_lens_host, batch, num_heads,
                                                 page_size, kv_dtype);
     if (st != MLA_OK) return st;
-    int sms = mla::device_sm_count();
+    const int sms = mla::device_sm_count();
     if (sms <= 0) return MLA_ERR_CUDA;
-    // head groups that share tiles run as clusters: no more CTAs than the
-    // device holds in clusters at once (a second wave would double the call)
-    if (kv_dtype == MLA_KV_FP8_E4M3 && num_heads % 32 == 0 &&
-        mla::tc_shares_tiles(32, num_heads / 32)) {
-        const int size = mla::tc_cluster_size(num_heads / 32);
-        const int clusters = mla::tc_cluster_capacity(size);
-        if (clusters > 0 && clusters * size < sms) sms = clusters * size;
-    }
     Schedule s;
     st = mla::build_schedule(kv_indptr_host, seq_lens_host, batch, num_heads, page_size,
                              kv_dtype, sms, s);

@@ -94,13 +94,6 @@ MLA_DEVINLINE void mma_commit(uint64_t* bar) {
                  :: "r"(smem_u32(bar)) : "memory");
 }
 
-// Arrives once on the mbarrier at `bar`'s offset in every CTA of `cta_mask`
-// when the MMAs issued so far by this thread have completed.
-MLA_DEVINLINE void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;\n" :: "r"(smem_u32(bar)), "h"(cta_mask) : "memory");
-}
 MLA_DEVINLINE void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 MLA_DEVINLINE void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
@@ -195,22 +188,6 @@ MLA_DEVINLINE void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes, 
         :: "r"(dst), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// Gathers rows r0..r3 of a 2-D tensor (tile::gather4: one box of `x`
-// channels per row, the tensor map's box one row high) into shared memory
-// at `dst` of every CTA in `cta_mask`, each copy completing as transaction
-// bytes on the mbarrier at `bar`'s offset in that CTA.  A row outside the
-// tensor reads as zeros.  `x` times the element size must be a multiple of
-// 16 bytes.
-MLA_DEVINLINE void tma_gather4_mc(uint32_t dst, const void* tensor_map, int32_t x, int4 rows, uint64_t* bar,
-                                  uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n"
-        :: "r"(dst), "l"(tensor_map), "r"(x), "r"(rows.x), "r"(rows.y), "r"(rows.z), "r"(rows.w),
-           "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
 // Has L2 fetch every 128-byte line of the `kBytes` bytes at `row` (one
 // prefetch per line, issued by the calling thread; nothing waits for them).
 template <int kBytes>
@@ -229,11 +206,6 @@ MLA_DEVINLINE void prefetch_row_l2(const void* row) {
 MLA_DEVINLINE uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-    return r;
-}
-MLA_DEVINLINE uint32_t cluster_nctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(r));
     return r;
 }
 // All threads of all CTAs of the cluster meet; shared-memory writes made
@@ -291,17 +263,6 @@ MLA_DEVINLINE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort
             return false;
         }
     }
-}
-
-// The wait of a role that issues work (MMAs, copies, barrier arrivals that
-// release a buffer): a phase seen complete after the CTA aborted counts as
-// failed.  After an abort the softmax warps keep arriving without having
-// waited for their inputs, and nothing may be issued on such an arrival (an
-// MMA over a stage that never landed, a re-armed barrier whose copies are
-// still outstanding).
-MLA_DEVINLINE bool mbar_wait_live(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags,
-                                  uint64_t limit_ns = 0) {
-    return mbar_wait(bar, parity, abort, flags, limit_ns) && *abort == 0;
 }
 
 }  // namespace tc

@@ -4,11 +4,8 @@ runs out sets MLA_FLAG_WAIT_TIMEOUT, makes the CTA abandon its work, let its
 copies and MMAs finish, free its tensor memory and exit.  The test shortens
 the limit through the library's test hook so that the first wait of every
 CTA runs out, checks the flag, restores the limit and checks that the next
-call on the same context is correct again.  After an abort no role that
-issues work acts on a barrier phase completed by the abandoned softmax
-loops.  Covered: 16-head CTAs (two query buffers, two segments in a CTA)
-and 32-head CTAs with one segment each, there as a cluster of two that
-share tiles (H = 64).
+call on the same context is correct again.  Covered: 16-head CTAs (two
+query buffers) and 32-head CTAs that each serve one segment.
 """
 import pytest
 import torch
@@ -45,16 +42,14 @@ def _timed_out_then_correct(run, check):
     check(out, lse)
 
 
-@pytest.mark.parametrize("heads,lens", [
-    (4, None),                           # 16-head CTAs, the tiny configuration
-    (64, [700, 90]),                     # clusters of two 32-head CTAs
-])
+@pytest.mark.parametrize("heads,lens", [(4, None), (64, [700, 90])])
 def test_decode_wait_timeout_flags_and_recovers(heads, lens):
+    """16-head CTAs (the tiny configuration) and 32-head CTAs (H = 64)."""
     if lens is None:
         w = W.make_workload("tiny")
     else:
         w = W.make_workload("concurrency", batch=len(lens), heads=heads, lens=lens,
-                            num_slots=5000, seed=71 + heads)
+                            num_slots=5000, seed=71)
     pool = oracle_pool(w)
     dpool = torch.from_numpy(pool).cuda()
     o_ref, lse_ref = oracle.decode_fp8(w.q_bf16, pool[:, :512], pool[:, 512:], w.kv_indptr,
@@ -66,4 +61,3 @@ def test_decode_wait_timeout_flags_and_recovers(heads, lens):
         return out, lse
 
     _timed_out_then_correct(run, lambda o, l: check_attention(o, l, o_ref, lse_ref, "after timeout"))
-

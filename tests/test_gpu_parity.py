@@ -209,7 +209,7 @@ def test_decode_large_head_full_size_sampled():
     (32, 2, [300, 77]),
     (48, 1, [513]),
     (64, 1, [2000, 5, 700, 64]),                   # 32-head CTAs in two head groups
-    (96, 8, [777, 64, 1, 130]),                    # clusters of three sharing tiles
+    (96, 8, [777, 64, 1, 130]),                    # three 32-head groups, paged
     (128, 64, [1000, 64, 3]),
 ])
 def test_decode_edge_shapes(heads, ps, lens):
@@ -225,8 +225,8 @@ def test_decode_edge_shapes(heads, ps, lens):
 
 @pytest.mark.parametrize("heads", [16, 64, 128])
 def test_decode_strided_q_and_separate_pools(heads):
-    """Padded c_kv and k_pe pools of their own (H = 64, 128: the head groups
-    of a token range gather through two row maps and share tiles)."""
+    """Padded c_kv and k_pe pools of their own, at 16 heads and at 64 and
+    128 (32-head CTAs, two and four head groups per token range)."""
     w = W.make_workload("concurrency", batch=3, heads=heads, lens=[200, 1, 777], num_slots=3000,
                         seed=5)
     pool = oracle_pool(w)
