@@ -107,8 +107,17 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kP2Scale = 32.f;            // P's second term is stored x 2^5
 constexpr uint32_t kP2ScaleF16x2 = 0x50005000u;   // 32.0 in both f16 halves
 constexpr int kCoefBytesPerRow = 12;        // per q image row: two fp32 multipliers, one int32 limit
-constexpr int kRing = 8;                    // published tiles' slot lists (and L2 prefetches) in flight
-static_assert(kRing > kStages, "the ring covers the tiles the stages hold");
+// Published tiles' slot lists (and L2 prefetches) in flight: the scheduler
+// runs at most this many tiles ahead of the softmax.  Measured on GB300:
+// 6 for 16-head CTAs (the batch-40 call 34.5 us, against 34.9 with 8 and
+// with 5, 34.7 with 7: fewer outstanding prefetches queue less in DRAM and
+// the tiles still land in time), 8 for 32-head CTAs (6 made the 4-token
+// extend 1.4 % and the 256-token one 2 % slower).
+constexpr int kRing = 8;                    // ring entries in shared memory (the deepest ring)
+template <int G>
+constexpr int ring_depth() { return G == 16 ? 6 : 8; }
+static_assert(ring_depth<16>() > kStages && ring_depth<32>() > kStages && ring_depth<32>() <= kRing,
+              "the ring covers the tiles the stages hold");
 
 // A CTA serves G = 16 or 32 heads (32 when H is a multiple of 32: one read of
 // a tile then feeds twice the heads, and an N = 64 MMA costs what N = 32 does).
@@ -341,7 +350,7 @@ __device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage
 }
 
 // cur: started by the caller (its first page entries already requested)
-template <bool E>
+template <bool E, int kR>
 __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                           TileCursor<E>& cur, int lane) {
     int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
@@ -350,8 +359,8 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     // publishes every tile as soon as its ring entry is free (the ring bounds
     // how far ahead of the softmax warps the prefetches run)
     for (int n = 0; cur.valid(); ++n) {
-        const int e = n % kRing;
-        const uint32_t u = static_cast<uint32_t>(n / kRing);
+        const int e = n % kR;
+        const uint32_t u = static_cast<uint32_t>(n / kR);
         int32_t sl[2];
         cur.rows(p, sl);
         cur.advance(p, lane);                         // the next tile's index loads fly meanwhile
@@ -373,7 +382,7 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     }
 }
 
-template <bool E>
+template <bool E, int kR>
 __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
                           int seg_lo, int seg_hi, int w, int lane) {
     const int32_t* ring = reinterpret_cast<const int32_t*>(base + kOffRing);
@@ -381,8 +390,8 @@ __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     for (int i = 0; i < total; ++i) {
         const int slot = i % kStages;
         const uint32_t u = static_cast<uint32_t>(i / kStages);
-        const int e = i % kRing;
-        if (!warp_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, abort, p.flags)) break;
+        const int e = i % kR;
+        if (!warp_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, abort, p.flags)) break;
         int32_t sl[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
@@ -872,8 +881,9 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             const int slot = i & 1;
             const uint32_t u = static_cast<uint32_t>(i) >> 1;
             // row validity from the scheduler's slot list (a -1 row is zero-filled)
-            const int e = i % kRing;
-            mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kRing) & 1, w.abort, w.flags);
+            constexpr int kR = ring_depth<G>();
+            const int e = i % kR;
+            mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, w.abort, w.flags);
             const bool valid = ring[e * kTT + w.srow] >= 0;
             __syncwarp();
             if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
@@ -1118,7 +1128,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
             mbar_init(&bars[Q_FREE + b], kSm + 1);
         }
         mbar_init(&bars[DONE], 2);
-        for (int e = 0; e < kRing; ++e) {
+        for (int e = 0; e < ring_depth<G>(); ++e) {
             mbar_init(&bars[SL_FULL + e], 1);
             mbar_init(&bars[SL_EMPTY + e], kFillWarps + 4 * S::kWgs);
         }
@@ -1133,9 +1143,9 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == S::kWarpSched) {
-        scheduler<E>(p, base, bars, abort, cur, lane);
+        scheduler<E, ring_depth<G>()>(p, base, bars, abort, cur, lane);
     } else if (warp < kFillWarps) {
-        fill_warp<E>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
+        fill_warp<E, ring_depth<G>()>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
     } else if (warp == kWarpMma || warp == S::kWarpPv) {
         if (lane == 0) {
             MmaCtx c;
