@@ -111,12 +111,14 @@ constexpr int kCoefBytesPerRow = 12;        // per q image row: two fp32 multipl
 // runs at most this many tiles ahead of the softmax.  Measured on GB300:
 // 6 for 16-head CTAs (the batch-40 call 34.5 us, against 34.9 with 8 and
 // with 5, 34.7 with 7: fewer outstanding prefetches queue less in DRAM and
-// the tiles still land in time), 8 for 32-head CTAs (6 made the 4-token
-// extend 1.4 % and the 256-token one 2 % slower).
-constexpr int kRing = 8;                    // ring entries in shared memory (the deepest ring)
-template <int G>
-constexpr int ring_depth() { return G == 16 ? 6 : 8; }
-static_assert(ring_depth<16>() > kStages && ring_depth<32>() > kStages && ring_depth<32>() <= kRing,
+// the tiles still land in time); for 32-head CTAs 8 in decode (12 made the
+// 128-head call 1.4 % slower) and 12 in extend (256-token extend 657 vs 663
+// us; 6 made the 4-token extend 1.4 % and the 256-token one 2 % slower).
+constexpr int kRing = 12;                   // ring entries in shared memory (the deepest ring)
+template <int G, bool E>
+constexpr int ring_depth() { return G == 16 ? 6 : (E ? 12 : 8); }
+static_assert(ring_depth<16, false>() > kStages && ring_depth<32, false>() > kStages &&
+                  ring_depth<32, true>() <= kRing,
               "the ring covers the tiles the stages hold");
 
 // A CTA serves G = 16 or 32 heads (32 when H is a multiple of 32: one read of
@@ -881,7 +883,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             const int slot = i & 1;
             const uint32_t u = static_cast<uint32_t>(i) >> 1;
             // row validity from the scheduler's slot list (a -1 row is zero-filled)
-            constexpr int kR = ring_depth<G>();
+            constexpr int kR = ring_depth<G, E>();
             const int e = i % kR;
             mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, w.abort, w.flags);
             const bool valid = ring[e * kTT + w.srow] >= 0;
@@ -1128,7 +1130,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
             mbar_init(&bars[Q_FREE + b], kSm + 1);
         }
         mbar_init(&bars[DONE], 2);
-        for (int e = 0; e < ring_depth<G>(); ++e) {
+        for (int e = 0; e < ring_depth<G, E>(); ++e) {
             mbar_init(&bars[SL_FULL + e], 1);
             mbar_init(&bars[SL_EMPTY + e], kFillWarps + 4 * S::kWgs);
         }
@@ -1143,9 +1145,9 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == S::kWarpSched) {
-        scheduler<E, ring_depth<G>()>(p, base, bars, abort, cur, lane);
+        scheduler<E, ring_depth<G, E>()>(p, base, bars, abort, cur, lane);
     } else if (warp < kFillWarps) {
-        fill_warp<E, ring_depth<G>()>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
+        fill_warp<E, ring_depth<G, E>()>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
     } else if (warp == kWarpMma || warp == S::kWarpPv) {
         if (lane == 0) {
             MmaCtx c;
