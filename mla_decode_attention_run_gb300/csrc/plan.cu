@@ -37,10 +37,10 @@ DecodeKernel pick_kernel(mla_kv_dtype_t dtype, int32_t) {
 int64_t min_tiles_per_cta(DecodeKernel) { return 2; }
 
 // tcgen05 schedule: requests' tiles in order, cut into CTA ranges so that the
-// largest CTA cost (tiles + kTcSegmentCost per segment) is as small as
+// largest CTA cost (tiles + seg_cost per segment) is as small as
 // possible: binary search on the cost cap, greedy fill under it.
-int64_t fill_under_cap(const int32_t* seq, int32_t B, int64_t tile, int64_t cap, int64_t max_ctas,
-                       Schedule* out, std::vector<int32_t>* segs_per_req) {
+int64_t fill_under_cap(const int32_t* seq, int32_t B, int64_t tile, int64_t seg_cost, int64_t cap,
+                       int64_t max_ctas, Schedule* out, std::vector<int32_t>* segs_per_req) {
     int64_t c = 0, cost = 0;
     bool any = false;
     if (out) out->cta_ptr.assign(1, 0);
@@ -48,7 +48,7 @@ int64_t fill_under_cap(const int32_t* seq, int32_t B, int64_t tile, int64_t cap,
         int64_t done = 0;
         const int64_t tiles = (seq[b] + tile - 1) / tile;
         while (done < tiles) {
-            const int64_t room = cap - cost - kTcSegmentCost;
+            const int64_t room = cap - cost - seg_cost;
             if (room < 1) {
                 if (cost == 0) return INT64_MAX;            // cap below one tile + segment
                 if (++c >= max_ctas) return INT64_MAX;
@@ -64,7 +64,7 @@ int64_t fill_under_cap(const int32_t* seq, int32_t B, int64_t tile, int64_t cap,
                                                    static_cast<int32_t>(t1), -1});
                 ++(*segs_per_req)[b];
             }
-            cost += kTcSegmentCost + k;
+            cost += seg_cost + k;
             done += k;
             any = true;
         }
@@ -72,8 +72,62 @@ int64_t fill_under_cap(const int32_t* seq, int32_t B, int64_t tile, int64_t cap,
     return any ? c + 1 : 0;
 }
 
-void build_cost_balanced(const int32_t* seq, int32_t B, int64_t tile, int64_t max_ctas, Schedule& s,
-                         std::vector<int32_t>& segs_per_req) {
+// The greedy fill at the smallest cap can leave CTAs unused (at a larger
+// segment cost it packs the ranges tighter).  More ranges never raise a
+// range's cost, so the ranges of highest cost are split at their middle tile
+// (a segment cut there becomes two segments of its request) until every CTA
+// has one: the largest cost stays the same or drops, and no SM idles.
+void split_costliest(Schedule& s, int64_t tile, int64_t seg_cost, int64_t max_ctas,
+                     std::vector<int32_t>& segs_per_req) {
+    std::vector<std::vector<int32_t>> ranges(s.num_ctas);
+    for (int32_t c = 0; c < s.num_ctas; ++c)
+        ranges[c].assign(s.segs.begin() + 4 * s.cta_ptr[c], s.segs.begin() + 4 * s.cta_ptr[c + 1]);
+    auto tiles_of = [&](const std::vector<int32_t>& r) {
+        int64_t t = 0;
+        for (size_t i = 0; i < r.size(); i += 4) t += (r[i + 2] - r[i + 1] + tile - 1) / tile;
+        return t;
+    };
+    auto cost_of = [&](const std::vector<int32_t>& r) {
+        return tiles_of(r) + seg_cost * static_cast<int64_t>(r.size() / 4);
+    };
+    while (static_cast<int64_t>(ranges.size()) < max_ctas) {
+        size_t top = 0;
+        for (size_t c = 1; c < ranges.size(); ++c)
+            if (cost_of(ranges[c]) > cost_of(ranges[top])) top = c;
+        const std::vector<int32_t> r = ranges[top];
+        const int64_t half = tiles_of(r) / 2;
+        if (half < 1) break;
+        std::vector<int32_t> left, right;
+        int64_t acc = 0;
+        for (size_t i = 0; i < r.size(); i += 4) {
+            const int32_t b = r[i], t0 = r[i + 1], t1 = r[i + 2];
+            const int64_t n = (t1 - t0 + tile - 1) / tile;
+            if (acc + n <= half) {
+                left.insert(left.end(), {b, t0, t1, -1});
+            } else if (acc >= half) {
+                right.insert(right.end(), {b, t0, t1, -1});
+            } else {                                   // cut this segment on a tile boundary
+                const int32_t cut = static_cast<int32_t>(t0 + (half - acc) * tile);
+                left.insert(left.end(), {b, t0, cut, -1});
+                right.insert(right.end(), {b, cut, t1, -1});
+                ++segs_per_req[b];
+            }
+            acc += n;
+        }
+        ranges[top] = left;
+        ranges.insert(ranges.begin() + static_cast<int64_t>(top) + 1, right);
+    }
+    s.segs.clear();
+    s.cta_ptr.assign(1, 0);
+    for (const auto& r : ranges) {
+        s.segs.insert(s.segs.end(), r.begin(), r.end());
+        s.cta_ptr.push_back(static_cast<int32_t>(s.segs.size() / 4));
+    }
+    s.num_ctas = static_cast<int32_t>(ranges.size());
+}
+
+void build_cost_balanced(const int32_t* seq, int32_t B, int64_t tile, int64_t seg_cost, int64_t max_ctas,
+                         Schedule& s, std::vector<int32_t>& segs_per_req) {
     int64_t n_tiles = 0, n_req = 0;
     for (int32_t b = 0; b < B; ++b) {
         n_tiles += (seq[b] + tile - 1) / tile;
@@ -85,17 +139,17 @@ void build_cost_balanced(const int32_t* seq, int32_t B, int64_t tile, int64_t ma
         s.cta_ptr.assign(1, 0);
         return;
     }
-    int64_t lo = (n_tiles + kTcSegmentCost * n_req + max_ctas - 1) / max_ctas;
-    if (lo < kTcSegmentCost + 1) lo = kTcSegmentCost + 1;
+    int64_t lo = (n_tiles + seg_cost * n_req + max_ctas - 1) / max_ctas;
+    if (lo < seg_cost + 1) lo = seg_cost + 1;
     // everything in one CTA: every request one segment (always feasible)
-    int64_t hi = n_tiles + kTcSegmentCost * n_req;
+    int64_t hi = n_tiles + seg_cost * n_req;
     if (hi < lo) hi = lo;
     while (lo < hi) {
         const int64_t mid = lo + (hi - lo) / 2;
-        if (fill_under_cap(seq, B, tile, mid, max_ctas, nullptr, nullptr) != INT64_MAX) hi = mid;
+        if (fill_under_cap(seq, B, tile, seg_cost, mid, max_ctas, nullptr, nullptr) != INT64_MAX) hi = mid;
         else lo = mid + 1;
     }
-    const int64_t used = fill_under_cap(seq, B, tile, lo, max_ctas, &s, &segs_per_req);
+    const int64_t used = fill_under_cap(seq, B, tile, seg_cost, lo, max_ctas, &s, &segs_per_req);
     if (used == INT64_MAX) {                                   // cannot happen with the bounds above
         s.segs.clear();
         s.num_ctas = 0;
@@ -106,6 +160,7 @@ void build_cost_balanced(const int32_t* seq, int32_t B, int64_t tile, int64_t ma
     s.num_ctas = static_cast<int32_t>(used);
     s.cta_ptr.resize(s.num_ctas + 1);
     s.cta_ptr[s.num_ctas] = static_cast<int32_t>(s.segs.size() / 4);
+    if (used < max_ctas) split_costliest(s, tile, seg_cost, max_ctas, segs_per_req);
 }
 
 // Workspace: partials (o, then lse) for part_rows rows each, then, on the
@@ -174,7 +229,7 @@ mla_status_t build_schedule(const int32_t* indptr, const int32_t* seq, int32_t B
 
     std::vector<int32_t> segs_per_req(B, 0);
     if (kernel == DecodeKernel::kTc) {
-        build_cost_balanced(seq, B, tile, ctas, s, segs_per_req);
+        build_cost_balanced(seq, B, tile, kTcSegmentCost, ctas, s, segs_per_req);
     } else {
         // request tile offsets in the concatenated tile list
         std::vector<int64_t> first_tile(B + 1, 0);
@@ -308,7 +363,7 @@ mla_status_t build_extend_schedule(const int32_t* qo, const int32_t* indptr, con
     std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) { return place[a] < place[b]; });
     std::vector<int32_t> len_o(nb), segs_o(nb, 0);
     for (int32_t j = 0; j < nb; ++j) len_o[j] = len[order[j]];
-    build_cost_balanced(len_o.data(), nb, kTcTileTokens, ctas, s, segs_o);
+    build_cost_balanced(len_o.data(), nb, kTcTileTokens, kTcExtendSegmentCost, ctas, s, segs_o);
     for (int32_t i = 0; i < s.n_segs(); ++i) s.segs[4 * i] = order[s.segs[4 * i]];
     std::vector<int32_t> segs_per_block(nb, 0);
     for (int32_t j = 0; j < nb; ++j) segs_per_block[order[j]] = segs_o[j];

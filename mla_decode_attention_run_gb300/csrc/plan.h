@@ -15,10 +15,12 @@ namespace mla {
 // kernel, and heads per CTA.
 constexpr int kTileTokens = 64;
 constexpr int kTcTileTokens = 64;
-// tcgen05 kernel: a segment (q fetch, pipeline refill, epilogue) costs about
-// as much CTA time as this many tiles (measured on GB300); the schedule
-// balances tiles + this per segment across CTAs
+// tcgen05 kernel: the schedule balances tiles + this many tiles per segment
+// (its q fetch, pipeline refill and epilogue) across CTAs.  Measured on
+// GB300: 2 for decode (the batch-40 call 34.3 us against 35.2-35.5 at 4 or
+// 5), 4 for extend (4-token extend 65.3 vs 66.5 us).
 constexpr int kTcSegmentCost = 2;
+constexpr int kTcExtendSegmentCost = 4;
 constexpr int kHeadsPerCta = 16;
 // tcgen05 path: per request and group of 16 heads, [q1;q2;q3] as the
 // shared-memory image the MMA reads (3 x 16 rows x 576 E4M3, swizzled)
