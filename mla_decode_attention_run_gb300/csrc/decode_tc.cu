@@ -166,7 +166,9 @@ constexpr int kOffLsum = kOffRed + 2 * 4 * kMaxG * 4;   // softmax denominators:
 constexpr int kOffCoef = kOffLsum + 4 * kMaxG * 4;      // per q buffer: 2 G multipliers, G limits
 constexpr int kOffFlag = kOffCoef + 2 * 16 * kCoefBytesPerRow;   // rescale votes: per warpgroup 2 x 4 warps
 constexpr int kOffMisc = kOffFlag + 64;     // TMEM base, abort flag
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+constexpr int kSegTab = 64;                 // segment records a CTA keeps in shared memory
+constexpr int kOffSegTab = kOffMisc + 16;   // kSegTab x 32 B
+constexpr int kSmemBytes = kOffSegTab + kSegTab * 32 + 1024;
 static_assert(Shape<16>::kQBufs * 16 * kCoefBytesPerRow <= 2 * 16 * kCoefBytesPerRow &&
                   Shape<32>::kQBufs * 32 * kCoefBytesPerRow <= 2 * 16 * kCoefBytesPerRow,
               "multiplier and limit space");
@@ -195,6 +197,12 @@ static_assert(NUM_BARS * 8 <= 512, "barrier space");
 struct Seg {
     int32_t b, req, t0, t1, part, ntiles;
 };
+// a segment table entry: the record and its request's first page-table entry
+struct alignas(16) SegEntry {
+    Seg s;
+    int32_t pages, pad;
+};
+static_assert(sizeof(SegEntry) == 32, "segment table entries");
 
 // E: extend plan (segments name query blocks); the decode kernels are
 // compiled without the indirection
@@ -212,10 +220,32 @@ __device__ __forceinline__ Seg load_seg(const DecodeParams& p, int si) {
     return s;
 }
 
-template <bool E>
-__device__ __forceinline__ int count_tiles(const DecodeParams& p, int lo, int hi) {
+// The CTA's segments lo .. hi - 1.  The first N of them are loaded into
+// shared memory once, before the roles start, so that no role waits on the
+// plan's dependent loads (record, then context length) at a switch between
+// segments; later ones are read from the plan.  16-head CTAs keep kSegTab
+// (batch-40 call 33.94 vs 34.18 us on GB300); 32-head CTAs none: at 128
+// registers a thread the table's code made that kernel spill more, and it
+// ran 12 % slower (256-token extend 780 vs 656 us).
+template <bool E, int N>
+struct SegView {
+    const SegEntry* tab;
+    int lo, hi;
+    __device__ __forceinline__ Seg at(const DecodeParams& p, int si) const {
+        if constexpr (N > 0) {
+            if (si - lo < N) return tab[si - lo].s;
+        }
+        return load_seg<E>(p, si);
+    }
+};
+
+template <int G>
+constexpr int seg_tab_entries() { return G == 16 ? kSegTab : 0; }
+
+template <bool E, int N>
+__device__ __forceinline__ int count_tiles(const DecodeParams& p, const SegView<E, N>& sv) {
     int n = 0;
-    for (int si = lo; si < hi; ++si) n += load_seg<E>(p, si).ntiles;
+    for (int si = sv.lo; si < sv.hi; ++si) n += sv.at(p, si).ntiles;
     return n;
 }
 
@@ -241,23 +271,35 @@ __device__ __forceinline__ void wg_bar(int g) {
 
 constexpr int32_t kNoRow = INT32_MIN;
 
+// The bounded wait of the roles of a CTA of G heads.  16-head CTAs wait with
+// whole warps, also in their MMA issuers, and use the polled form; 32-head
+// CTAs (512 threads at 128 registers, whose speed moved by 5-18 % with the
+// shape of their code) keep the single-lane issuers and mbar_wait.
+template <int G>
+__device__ __forceinline__ bool bwait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags) {
+    if constexpr (G == 16) return mbar_wait_polled(bar, parity, abort, flags);
+    else return mbar_wait(bar, parity, abort, flags);
+}
+
 // A wait made by every lane of a warp that then acts together (shuffles,
 // warp barriers): the warp goes on only if every lane's wait succeeded, so
 // that after an abort no lane leaves the loop while the others stay in it.
+template <int G>
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* flags) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, flags));
+    return __all_sync(0xffffffffu, bwait<G>(bar, parity, abort, flags));
 }
 
 // Cursor over the tiles of a CTA's segments, with the raw page entries of
 // rows 2 lane, 2 lane + 1 of one tile.
-template <bool E>
+template <bool E, int N>
 struct TileCursor {
     int si, seg_hi, it;
     Seg sg;
     const int32_t* pages;
     int32_t pg[2];                      // page entry, or kNoRow past the context
     int32_t t[2];                       // token index of each row
+    SegView<E, N> sv;                   // the shared segment table (tab null until it is loaded)
 
     // first: the first segment's t0, t1 and page-table offset when the
     // launch carries them (its page entries are then requested before the
@@ -265,6 +307,7 @@ struct TileCursor {
     __device__ void init(const DecodeParams& p, int lo, int hi, const int4* first, int lane) {
         si = lo;
         seg_hi = hi;
+        sv.tab = nullptr;
         if (first != nullptr && si < seg_hi) {
             pages = p.indices + first->z;
             sg.t0 = first->x;
@@ -284,8 +327,14 @@ struct TileCursor {
     // table either way.
     __device__ void seek(const DecodeParams& p, int lane) {
         while (si < seg_hi) {
-            pages = p.indices + p.seg_pages[si];
-            sg = load_seg<E>(p, si);
+            if (N > 0 && sv.tab != nullptr && si - sv.lo < N) {
+                const SegEntry& e = sv.tab[si - sv.lo];
+                sg = e.s;
+                pages = p.indices + e.pages;
+            } else {
+                pages = p.indices + p.seg_pages[si];
+                sg = load_seg<E>(p, si);
+            }
             it = 0;
             prefetch(p, lane);
             if (sg.ntiles > 0) break;
@@ -352,10 +401,11 @@ __device__ __forceinline__ void fill_share(const DecodeParams& p, uint8_t* stage
 }
 
 // cur: started by the caller (its first page entries already requested)
-template <bool E, int kR>
+template <int G, bool E, int kR, int N>
 __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                          TileCursor<E>& cur, int lane) {
+                          TileCursor<E, N>& cur, const SegView<E, N>& sv, int lane) {
     int32_t* ring = reinterpret_cast<int32_t*>(base + kOffRing);
+    cur.sv = sv;
     // one prefetch sweep per row when k_pe follows c_kv in the same row
     const bool joint = p.kpe == p.ckv + kDCkv && p.kpe_stride == p.ckv_stride;
     // publishes every tile as soon as its ring entry is free (the ring bounds
@@ -366,7 +416,7 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
         int32_t sl[2];
         cur.rows(p, sl);
         cur.advance(p, lane);                         // the next tile's index loads fly meanwhile
-        if (!warp_wait(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
+        if (!warp_wait<G>(&bars[SL_EMPTY + e], (u & 1) ^ 1, abort, p.flags)) break;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             if (sl[q] < 0) continue;
@@ -384,22 +434,22 @@ __device__ void scheduler(const DecodeParams& p, uint8_t* base, uint64_t* bars, 
     }
 }
 
-template <bool E, int kR>
+template <int G, bool E, int kR, int N>
 __device__ void fill_warp(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                          int seg_lo, int seg_hi, int w, int lane) {
+                          const SegView<E, N>& sv, int w, int lane) {
     const int32_t* ring = reinterpret_cast<const int32_t*>(base + kOffRing);
-    const int total = count_tiles<E>(p, seg_lo, seg_hi);
+    const int total = count_tiles<E>(p, sv);
     for (int i = 0; i < total; ++i) {
         const int slot = i % kStages;
         const uint32_t u = static_cast<uint32_t>(i / kStages);
         const int e = i % kR;
-        if (!warp_wait(&bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, abort, p.flags)) break;
+        if (!warp_wait<G>(&bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, abort, p.flags)) break;
         int32_t sl[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) sl[q] = ring[e * kTT + lane + 32 * q];
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[SL_EMPTY + e]);
-        if (!warp_wait(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
+        if (!warp_wait<G>(&bars[KV_EMPTY + slot], (u & 1) ^ 1, abort, p.flags)) break;
         fill_share(p, base + kOffStage + slot * kStage, sl, w, lane);
         mbar_arrive_cp_async(&bars[KV_FULL + slot]);
     }
@@ -424,8 +474,15 @@ __device__ __forceinline__ uint64_t desc_at(uint64_t base_desc, uint32_t byte_of
     return base_desc + static_cast<uint64_t>(byte_offset >> 4);
 }
 
+// 16-head CTAs issue their MMAs from whole warps (one elected lane issues
+// and commits; the operands, computed by the warp, stay warp-uniform): the
+// batch-40 call 33.7 vs 34.2 us on GB300.  32-head CTAs issue from one lane.
 template <int G>
-__device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
+constexpr bool warp_issue() { return G == 16; }
+
+// q_done: the segment's last tile (its q buffer is released with it).
+template <int G>
+__device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs, bool q_done) {
     using S = Shape<G>;
     const int slot = i & 1;
     const uint32_t stage = c.sbase + kOffStage + (i % kStages) * kStage;
@@ -437,15 +494,19 @@ __device__ __forceinline__ void issue_qk(const MmaCtx& c, int i, int qs) {
     const uint64_t a64 = smem_desc(stage + 4 * kBlk, 16, 512, kSwizzle64B);
     const uint64_t b64 = smem_desc(qb + 4 * S::kQBlk, 16, 512, kSwizzle64B);
     const uint32_t d = c.tmem + kColS + S::kSCols * slot;
+    if (!warp_issue<G>() || elect_one()) {
 #pragma unroll
-    for (int ks = 0; ks < kKSteps; ++ks) {
-        const uint64_t a = ks < 16 ? desc_at(a128, (ks >> 2) * kBlk + (ks & 3) * 32)
-                                   : desc_at(a64, (ks - 16) * 32);
-        const uint64_t b = ks < 16 ? desc_at(b128, (ks >> 2) * S::kQBlk + (ks & 3) * 32)
-                                   : desc_at(b64, (ks - 16) * 32);
-        mma_e4m3(d, a, b, c.idesc_qk, ks > 0);
+        for (int ks = 0; ks < kKSteps; ++ks) {
+            const uint64_t a = ks < 16 ? desc_at(a128, (ks >> 2) * kBlk + (ks & 3) * 32)
+                                       : desc_at(a64, (ks - 16) * 32);
+            const uint64_t b = ks < 16 ? desc_at(b128, (ks >> 2) * S::kQBlk + (ks & 3) * 32)
+                                       : desc_at(b64, (ks - 16) * 32);
+            mma_e4m3(d, a, b, c.idesc_qk, ks > 0);
+        }
+        mma_commit(&c.bars[S_FULL + slot]);
+        if (q_done) mma_commit(&c.bars[Q_FREE + qs]);   // q buffer done
     }
-    mma_commit(&c.bars[S_FULL + slot]);
+    if constexpr (warp_issue<G>()) __syncwarp();
 }
 
 // PV of tile j into O buffer `ob`; the segment's first tile overwrites it.
@@ -459,97 +520,104 @@ __device__ __forceinline__ void issue_pv(const MmaCtx& c, int j, int ob, bool fi
     const uint64_t a0 = smem_desc(c.sbase + kOffStage + kv * kStage, kBlk, 1024, kSwizzle128B);
     const uint64_t b0 = smem_desc(c.sbase + kOffP + (j & 1) * S::kPBytes, 128, kPUnit, kSwizzleNone);
     const uint32_t d = c.tmem + S::kColO + 4 * S::kN * ob;
+    if (!warp_issue<G>() || elect_one()) {
 #pragma unroll
-    for (int mb = 0; mb < 4; ++mb) {
+        for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-        for (int ks = 0; ks < kTT / 32; ++ks)
-            mma_e4m3(d + S::kN * mb, desc_at(a0, mb * kBlk + ks * 32 * 128), desc_at(b0, ks * 32 * 16),
-                     c.idesc_pv, ks > 0 || !first);
+            for (int ks = 0; ks < kTT / 32; ++ks)
+                mma_e4m3(d + S::kN * mb, desc_at(a0, mb * kBlk + ks * 32 * 128), desc_at(b0, ks * 32 * 16),
+                         c.idesc_pv, ks > 0 || !first);
+        }
+        mma_commit(&c.bars[PV_DONE + (j & 1)]);
+        mma_commit(&c.bars[KV_EMPTY + kv]);   // the stage may be refilled
     }
-    mma_commit(&c.bars[PV_DONE + (j & 1)]);
-    mma_commit(&c.bars[KV_EMPTY + kv]);       // the stage may be refilled
+    if constexpr (warp_issue<G>()) __syncwarp();
 }
 
 // Position in the CTA's tile sequence: segment ordinal k and tile it of it.
-template <bool E>
+template <bool E, int N>
 struct SegWalk {
-    int si, seg_hi, it, k;
+    int si, it, k;
     Seg sg;
-    __device__ void init(const DecodeParams& p, int lo, int hi) {
-        si = lo;
-        seg_hi = hi;
+    __device__ void init(const DecodeParams& p, const SegView<E, N>& sv) {
+        si = sv.lo;
         it = 0;
         k = 0;
-        while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
+        while (si < sv.hi && (sg = sv.at(p, si)).ntiles == 0) ++si;
     }
-    __device__ void advance(const DecodeParams& p) {
+    __device__ void advance(const DecodeParams& p, const SegView<E, N>& sv) {
         if (++it == sg.ntiles) {
             it = 0;
             ++k;
             ++si;
-            while (si < seg_hi && (sg = load_seg<E>(p, si)).ntiles == 0) ++si;
+            while (si < sv.hi && (sg = sv.at(p, si)).ntiles == 0) ++si;
         }
     }
 };
 
-// Two issuing threads: one sends QK^T of the tiles in order, the other PV.
-// A thread waits for each MMA it issues to be accepted, so with one issuer the
-// PV of tile i queued behind QK^T of tile i + 1 (and freed its stage late);
-// with two, each goes out as soon as its inputs are ready.  QK^T needs its
-// stage full, so it runs at most a stage ahead of PV by construction.
+// Two issuers: one sends QK^T of the tiles in order, the other PV.  A thread
+// waits for each MMA it issues to be accepted, so with one issuer the PV of
+// tile i queued behind QK^T of tile i + 1 (and freed its stage late); with
+// two, each goes out as soon as its inputs are ready.  QK^T needs its stage
+// full, so it runs at most a stage ahead of PV by construction.  A warp that
+// issues as a whole waits with warp_wait, so that its lanes agree.
+template <int G>
+__device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, const MmaCtx& c) {
+    if constexpr (warp_issue<G>()) return warp_wait<G>(bar, parity, c.abort, c.flags);
+    else return bwait<G>(bar, parity, c.abort, c.flags);
+}
+
 template <int G, bool E>
-__device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
+__device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<E, seg_tab_entries<G>()>& sv) {
     using S = Shape<G>;
     int total = 0;
-    for (int si = seg_lo; si < seg_hi; ++si) {
-        const Seg sg = load_seg<E>(p, si);
-        if (sg.ntiles == 0 && sg.t1 > sg.t0) raise_flag(p.flags, MLA_FLAG_PLAN_MISMATCH);
+    for (int si = sv.lo; si < sv.hi; ++si) {
+        const Seg sg = sv.at(p, si);
+        if (sg.ntiles == 0 && sg.t1 > sg.t0 && (!warp_issue<G>() || (threadIdx.x & 31) == 0))
+            raise_flag(p.flags, MLA_FLAG_PLAN_MISMATCH);
         total += sg.ntiles;
     }
-    SegWalk<E> wq;
-    wq.init(p, seg_lo, seg_hi);
+    SegWalk<E, seg_tab_entries<G>()> wq;
+    wq.init(p, sv);
     for (int qk = 0; qk < total; ++qk) {
         const int slot = qk & 1;
         const int qs = wq.k % S::kQBufs;
-        if (wq.it == 0 &&
-            !mbar_wait(&c.bars[Q_FULL + qs], static_cast<uint32_t>(wq.k / S::kQBufs) & 1, c.abort, c.flags))
+        if (wq.it == 0 && !issuer_wait<G>(&c.bars[Q_FULL + qs], static_cast<uint32_t>(wq.k / S::kQBufs) & 1, c))
             break;
-        if (!mbar_wait(&c.bars[KV_FULL + qk % kStages], static_cast<uint32_t>(qk / kStages) & 1, c.abort, c.flags))
-            break;
-        if (!mbar_wait(&c.bars[S_FREE + slot], ((static_cast<uint32_t>(qk) >> 1) & 1) ^ 1, c.abort, c.flags))
-            break;
+        if (!issuer_wait<G>(&c.bars[KV_FULL + qk % kStages], static_cast<uint32_t>(qk / kStages) & 1, c)) break;
+        if (!issuer_wait<G>(&c.bars[S_FREE + slot], ((static_cast<uint32_t>(qk) >> 1) & 1) ^ 1, c)) break;
         fence_after_sync();
         fence_proxy_async_smem();
-        issue_qk<G>(c, qk, qs);
-        if (wq.it == wq.sg.ntiles - 1) mma_commit(&c.bars[Q_FREE + qs]);   // q buffer done
-        wq.advance(p);
+        issue_qk<G>(c, qk, qs, wq.it == wq.sg.ntiles - 1);
+        wq.advance(p, sv);
     }
     // every MMA issued so far has completed before TMEM may be released
-    mma_commit(&c.bars[DONE]);
+    if (!warp_issue<G>() || elect_one()) mma_commit(&c.bars[DONE]);
+    if constexpr (warp_issue<G>()) __syncwarp();
     volatile int never = 0;
     mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
 }
 
 template <int G, bool E>
-__device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, int seg_lo, int seg_hi) {
+__device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<E, seg_tab_entries<G>()>& sv) {
     using S = Shape<G>;
-    const int total = count_tiles<E>(p, seg_lo, seg_hi);
-    SegWalk<E> wp;
-    wp.init(p, seg_lo, seg_hi);
+    const int total = count_tiles<E>(p, sv);
+    SegWalk<E, seg_tab_entries<G>()> wp;
+    wp.init(p, sv);
     for (int pv = 0; pv < total; ++pv) {
         const int ob = wp.k % S::kOBufs;
-        if (!mbar_wait(&c.bars[P_FULL + (pv & 1)], (static_cast<uint32_t>(pv) >> 1) & 1, c.abort, c.flags)) break;
+        if (!issuer_wait<G>(&c.bars[P_FULL + (pv & 1)], (static_cast<uint32_t>(pv) >> 1) & 1, c)) break;
         // a segment's first PV overwrites its O buffer: the segment that used
         // it before has been read out
-        if (wp.it == 0 &&
-            !mbar_wait(&c.bars[O_FREE + ob], (static_cast<uint32_t>(wp.k / S::kOBufs) & 1) ^ 1, c.abort, c.flags))
+        if (wp.it == 0 && !issuer_wait<G>(&c.bars[O_FREE + ob], (static_cast<uint32_t>(wp.k / S::kOBufs) & 1) ^ 1, c))
             break;
         fence_after_sync();
         fence_proxy_async_smem();
         issue_pv<G>(c, pv, ob, wp.it == 0);
-        wp.advance(p);
+        wp.advance(p, sv);
     }
-    mma_commit(&c.bars[DONE]);
+    if (!warp_issue<G>() || elect_one()) mma_commit(&c.bars[DONE]);
+    if constexpr (warp_issue<G>()) __syncwarp();
     volatile int never = 0;
     mbar_wait(&c.bars[DONE], 0, &never, c.flags, 1000000000ull);
 }
@@ -735,17 +803,17 @@ __global__ void __maxnreg__(56) mla_q_split_kernel(const DecodeParams p) {
 // multipliers) once the split kernel has finished.
 template <int G, bool E>
 __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                        int seg_lo, int seg_hi, int lane) {
+                        const SegView<E, seg_tab_entries<G>()>& sv, int lane) {
     using S = Shape<G>;
     if (lane != 0) return;
     griddep_wait();                                 // the q images are complete
     int k = 0;
-    for (int si = seg_lo; si < seg_hi; ++si) {
-        const Seg sg = load_seg<E>(p, si);
+    for (int si = sv.lo; si < sv.hi; ++si) {
+        const Seg sg = sv.at(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k % S::kQBufs;
         const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
-        if (!mbar_wait(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
+        if (!bwait<G>(&bars[Q_FREE + qs], (qu & 1) ^ 1, abort, p.flags)) break;
         // After an abort the softmax warps keep arriving on Q_FREE without
         // the QK^T commit, so a phase can complete before the buffer's last
         // copy has landed; a second copy (and arrive.expect_tx) on Q_FULL
@@ -847,7 +915,8 @@ template <int V>
 __device__ __forceinline__ bool half_reduce_writer(int lane) { return V == 16 || (lane & 1) == 0; }
 
 template <int G, bool E>
-__device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, int seg_hi, int head0) {
+__device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<E, seg_tab_entries<G>()>& sv,
+                           int head0) {
     using S = Shape<G>;
     constexpr int kHL = 8;                          // heads per lane
     float* red = reinterpret_cast<float*>(w.base + kOffRed);
@@ -860,13 +929,13 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
     // at named barriers, so all of them run the loops to the end; once the
     // abort flag is set every wait returns at once and the results are void.
     int i = 0, k = 0;
-    for (int si = seg_lo; si < seg_hi; ++si) {
-        const Seg sg = load_seg<E>(p, si);
+    for (int si = sv.lo; si < sv.hi; ++si) {
+        const Seg sg = sv.at(p, si);
         if (sg.ntiles == 0) continue;
         const int qs = k % S::kQBufs;
         const uint32_t qu = static_cast<uint32_t>(k / S::kQBufs);
         const uint32_t ocol = S::kColO + 4 * S::kN * (k % S::kOBufs);
-        mbar_wait(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags);
+        bwait<G>(&w.bars[Q_FULL + qs], qu & 1, w.abort, w.flags);
         // the segment's score multipliers and causal limits stay in shared
         // memory (its q buffer is released at the end of the segment)
         const float* coef = coefs + qs * 3 * G;      // first two terms' multipliers
@@ -888,11 +957,11 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
             // row validity from the scheduler's slot list (a -1 row is zero-filled)
             constexpr int kR = ring_depth<G, E>();
             const int e = i % kR;
-            mbar_wait(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, w.abort, w.flags);
+            bwait<G>(&w.bars[SL_FULL + e], static_cast<uint32_t>(i / kR) & 1, w.abort, w.flags);
             const bool valid = ring[e * kTT + w.srow] >= 0;
             __syncwarp();
             if (w.lane == 0) mbar_arrive(&w.bars[SL_EMPTY + e]);
-            mbar_wait(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
+            bwait<G>(&w.bars[S_FULL + slot], u & 1, w.abort, w.flags);
             fence_after_sync();
             // the warp's 16 token rows sit in lanes 0-15 of its TMEM quadrant:
             // threads 0-15 read heads h0 .. h0 + 7 of their row, threads 16-31
@@ -960,14 +1029,14 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
                         a_all[kHL + j] = __shfl_sync(0xffffffffu, alpha[j], 16);
                     }
                     const int j = i - 1;
-                    mbar_wait(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort, w.flags);
+                    bwait<G>(&w.bars[PV_DONE + (j & 1)], (static_cast<uint32_t>(j) >> 1) & 1, w.abort, w.flags);
                     fence_after_sync();
                     rescale_o<G>(w, ocol, a_all);
                 }
             }
             // P = 2^(s - m) <= 2^kTau, stored as two E4M3 terms of p * kPScale;
             // its buffer was last read by PV(i - 2)
-            if (i >= 2) mbar_wait(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags);
+            if (i >= 2) bwait<G>(&w.bars[PV_DONE + slot], (u & 1) ^ 1, w.abort, w.flags);
             uint32_t pk1[kHL / 4], pk2[kHL / 4];
 #pragma unroll
             for (int e2 = 0; e2 < kHL / 4; ++e2) {
@@ -1027,7 +1096,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, int seg_lo, in
         }
         wg_bar(w.wg);                               // lsum is reused by the next segment
         const int jl = i - 1;                       // the segment's last tile
-        mbar_wait(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
+        bwait<G>(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
         // output rows row0 .. row0 + nrows - 1; a partial slot holds
         // p.part_rows rows, this CTA's from prow0
@@ -1109,8 +1178,14 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
     const bool ranged = static_cast<int>(blockIdx.x) < ranges.n;
     const int seg_lo = ranged ? ranges.seg[blockIdx.x] : p.cta_ptr[blockIdx.x];
     const int seg_hi = ranged ? ranges.seg[blockIdx.x + 1] : p.cta_ptr[blockIdx.x + 1];
+    // the segment table: one thread per segment, visible after the barrier below
+    constexpr int kTab = seg_tab_entries<G>();
+    SegEntry* segtab = reinterpret_cast<SegEntry*>(base + kOffSegTab);
+    if (tid < kTab && seg_lo + tid < seg_hi)
+        segtab[tid] = SegEntry{load_seg<E>(p, seg_lo + tid), p.seg_pages[seg_lo + tid], 0};
+    const SegView<E, kTab> sv{segtab, seg_lo, seg_hi};
     // the scheduler requests its first page entries while the CTA sets up
-    TileCursor<E> cur;
+    TileCursor<E, kTab> cur;
     if (warp == S::kWarpSched) cur.init(p, seg_lo, seg_hi, ranged ? &ranges.first[blockIdx.x] : nullptr, lane);
 
     if (tid == 0) {
@@ -1148,11 +1223,11 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
     const int head0 = blockIdx.y * G;             // heads head0 .. head0 + G - 1 of every request
 
     if (warp == S::kWarpSched) {
-        scheduler<E, ring_depth<G, E>()>(p, base, bars, abort, cur, lane);
+        scheduler<G, E, ring_depth<G, E>()>(p, base, bars, abort, cur, sv, lane);
     } else if (warp < kFillWarps) {
-        fill_warp<E, ring_depth<G, E>()>(p, base, bars, abort, seg_lo, seg_hi, warp, lane);
+        fill_warp<G, E, ring_depth<G, E>()>(p, base, bars, abort, sv, warp, lane);
     } else if (warp == kWarpMma || warp == S::kWarpPv) {
-        if (lane == 0) {
+        if (warp_issue<G>() || lane == 0) {
             MmaCtx c;
             c.sbase = smem_u32(base);
             c.tmem = tmem;
@@ -1161,12 +1236,12 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
             c.bars = bars;
             c.abort = abort;
             c.flags = p.flags;
-            if (warp == kWarpMma) qk_issuer<G, E>(p, c, seg_lo, seg_hi);
-            else pv_issuer<G, E>(p, c, seg_lo, seg_hi);
+            if (warp == kWarpMma) qk_issuer<G, E>(p, c, sv);
+            else pv_issuer<G, E>(p, c, sv);
         }
-        __syncwarp();
+        if constexpr (!warp_issue<G>()) __syncwarp();
     } else if (warp == kWarpQ) {
-        q_fetch<G, E>(p, base, bars, abort, seg_lo, seg_hi, lane);
+        q_fetch<G, E>(p, base, bars, abort, sv, lane);
     } else {                                      // warps S::kWarpWg ..: softmax warpgroups
         WgCtx w;
         w.base = base;
@@ -1182,7 +1257,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
         w.h0 = 16 * w.wg;
         w.hb = w.h0 + (lane >> 4) * 8;
         w.lane = lane;
-        softmax_wg<G, E>(p, w, seg_lo, seg_hi, head0);
+        softmax_wg<G, E>(p, w, sv, head0);
     }
     fence_before_sync();
     __syncthreads();
@@ -1239,7 +1314,8 @@ cudaError_t launch_g(const DecodeParams& p, const TcRanges& ranges, int grid, cu
 
 cudaError_t set_decode_wait_limit(uint64_t limit_ns) {
     const uint64_t v = limit_ns ? limit_ns : kDefaultWaitLimitNs;
-    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+    const cudaError_t e = cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+    return e != cudaSuccess ? e : cudaMemcpyToSymbol(c_wait_limit_ns, &v, sizeof(v));
 }
 
 cudaError_t launch_decode_tc(const DecodeParams& p, const TcRanges& ranges, int grid,

@@ -2,9 +2,10 @@
 GPU: every wait of a CTA on an in-kernel barrier is bounded, and a wait that
 runs out sets MLA_FLAG_WAIT_TIMEOUT, makes the CTA abandon its work, let its
 copies and MMAs finish, free its tensor memory and exit.  The test shortens
-the limit through the library's test hook so that the first wait of every
-CTA runs out, checks the flag, restores the limit and checks that the next
-call on the same context is correct again.  Covered: 16-head CTAs (two
+the limit through the library's test hook to 1 ns, so that the first wait
+of a CTA that finds its phase incomplete runs out, checks the flag,
+restores the limit and checks that the next call on the same context is
+correct again.  Covered: 16-head CTAs (two
 query buffers) and 32-head CTAs that each serve one segment.
 """
 import pytest
