@@ -178,17 +178,6 @@ MLA_DEVINLINE bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
     return ok != 0;
 }
-// The same test with the thread's suspension bounded by `kSuspendHintNs`
-// (completion of the phase still wakes it at once).
-constexpr uint32_t kSuspendHintNs = 500;
-MLA_DEVINLINE bool mbar_try_wait_bounded(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendHintNs) : "memory");
-    return ok != 0;
-}
 // Tests the phase without suspending the thread.
 MLA_DEVINLINE bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
@@ -286,12 +275,14 @@ MLA_DEVINLINE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort
 
 // mbar_wait's contract, for warps that wait as a whole: the first test does
 // not suspend, and the clock starts when it finds the phase incomplete; the
-// thread then sleeps in try_wait at most kSuspendHintNs at a time (a whole
-// warp's try_wait may otherwise sleep through a wait of microseconds).  A
-// limit under kPollLimitNs (the test hook's) is checked between tests that
-// do not suspend, so that it runs out on every wait that has to wait.
-// Measured on GB300 with 16-head CTAs: 33.7 us per batch-40 call, against
-// 34.0 with mbar_wait and 37.1 with a bounded try_wait as the first test.
+// thread then waits in try_wait.  A limit under kPollLimitNs (the test
+// hook's) is checked between tests that do not suspend, so that it runs out
+// on every wait that has to wait, however long the hardware lets a thread
+// sleep in try_wait (a whole warp's try_wait can sleep through a wait of
+// microseconds).  Measured on GB300 with 16-head CTAs: 33.2 us per batch-40
+// call, against 34.0 with mbar_wait, 33.6 with try_wait's suspension bounded
+// by a hint (0.5, 2 or 8 us) and 37.1 with a bounded try_wait as the first
+// test.
 constexpr uint64_t kPollLimitNs = 1000000;
 MLA_DEVINLINE bool mbar_wait_polled(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags) {
     if (mbar_test_wait(bar, parity)) return true;
@@ -299,7 +290,7 @@ MLA_DEVINLINE bool mbar_wait_polled(uint64_t* bar, uint32_t parity, volatile int
     const uint64_t t0 = global_ns();
     const bool poll = lim < kPollLimitNs;
     while (true) {
-        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait_bounded(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (global_ns() - t0 > lim) {
             *abort = 1;
