@@ -245,6 +245,24 @@ def test_decode_strided_q_and_separate_pools(heads):
     check_attention(out, lse, o_ref, lse_ref, f"strided H={heads}")
 
 
+def test_decode_many_short_requests_past_the_segment_table():
+    """12,000 requests of 1-99 tokens: every 16-head CTA serves 73-82
+    segments, more than the 64 it keeps in shared memory, so it reads the
+    rest from the plan as it reaches them."""
+    B = 12000
+    lens = np.random.default_rng(5).integers(1, 100, B)
+    w = W.make_workload("concurrency", batch=B, heads=16, lens=list(lens), num_slots=650000, seed=91)
+    sched, info = M.mla_decode_schedule(w.kv_indptr, w.seq_lens, B, 16, 1, M.MLA_KV_FP8_E4M3)
+    per_cta = np.bincount(np.asarray(sched)[:, 0])
+    assert info["kernel"] == 1 and per_cta.min() > 64
+    pool = oracle_pool(w)
+    out, lse, flags = _decode_case(w, pool)
+    assert flags == 0
+    o_ref, lse_ref = oracle.decode_fp8(w.q_bf16, pool[:, :512], pool[:, 512:], w.kv_indptr,
+                                       w.kv_indices, w.seq_lens, 1, w.k_scale, w.softmax_scale)
+    check_attention(out, lse, o_ref, lse_ref, "12,000 short requests")
+
+
 def test_decode_is_deterministic():
     w = W.make_workload("concurrency", batch=6, num_slots=60000, seed=9)
     pool = torch.from_numpy(oracle_pool(w)).cuda()
