@@ -122,6 +122,12 @@ MLA_DEVINLINE void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
+// The same for 4 columns.
+MLA_DEVINLINE void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
 // M = 64 accumulators keep a warp's 16 rows in lanes 0-15 of its lane
 // quadrant.  This load gives threads 0-15 those 16 lanes at columns
 // col .. col + N - 1 and threads 16-31 the same lanes at columns
