@@ -1090,11 +1090,15 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
         wg_bar(w.wg);
         // inverse denominators of the warpgroup's heads h0 + t; a head whose q
         // held an infinity or a NaN has NaN multipliers: its output and lse
-        // become NaN (nothing else of it is NaN).  Compact form: one lane per
-        // head, through shared memory, for the rolled store loop below.
-        float inv[compact_epilogue<G, E>() ? 1 : 16];
+        // become NaN (nothing else of it is NaN).  One lane per head, through
+        // shared memory, rather than all 16 in every thread (16 divisions of
+        // code each): 16-head CTAs (batch-40 call 32.7 vs 33.3 us on GB300)
+        // and the rolled store of 32-head decode; 32-head extend keeps them
+        // in registers.
+        constexpr bool kSharedInv = compact_epilogue<G, E>() || G == 16;
+        float inv[kSharedInv ? 1 : 16];
         float* invs = reinterpret_cast<float*>(w.base + kOffInv) + w.h0;
-        if constexpr (compact_epilogue<G, E>()) {
+        if constexpr (kSharedInv) {
             if (w.wq == 0 && w.lane < 16) {
                 const int h = w.h0 + w.lane;
                 const float L = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h];
@@ -1175,7 +1179,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     if (w.h0 + t >= nrows) break;
-                    out[t * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[t] * inv[t]));
+                    out[t * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[t] * (kSharedInv ? invs[t] : inv[t])));
                 }
             } else {
                 float* po = p.part_o + (int64_t(sg.part) * p.part_rows + prow0 + w.h0) * kDCkv + ch;
@@ -1183,7 +1187,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     if (w.h0 + t >= nrows) break;
-                    st_f32_hint(po + t * kDCkv, o[t] * inv[t], keep);
+                    st_f32_hint(po + t * kDCkv, o[t] * (kSharedInv ? invs[t] : inv[t]), keep);
                 }
             }
         }
