@@ -1112,10 +1112,14 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
                 inv[t] = (L > 0.f ? p.k_scale / L : 0.f) + (coef[h] - coef[h]);
             }
         }
-        float Lmine[kHL];                           // this lane's heads, for the lse
+        // denominators for the lse: 16-head CTAs one per lane (head hb + (lane
+        // & 7), stored by lanes 0-7 and 16-23 of the first warp), the others
+        // all kHL of the lane's heads (stored by lanes 0 and 16)
+        constexpr int kLse = G == 16 ? 1 : kHL;
+        float Lmine[kLse];
 #pragma unroll
-        for (int j = 0; j < kHL; ++j) {
-            const int h = w.hb + j;
+        for (int j = 0; j < kLse; ++j) {
+            const int h = w.hb + (kLse == 1 ? (w.lane & 7) : j);
             Lmine[j] = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h] + (coef[h] - coef[h]);
         }
         wg_bar(w.wg);                               // lsum is reused by the next segment; invs is written
@@ -1195,7 +1199,24 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
         fence_before_sync();
         mbar_arrive(&w.bars[O_FREE + (k % S::kOBufs)]);   // a later segment may overwrite O
         mbar_arrive(&w.bars[Q_FREE + qs]);
-        if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb + kHL - 1
+        if constexpr (G == 16) {
+            // one lane per head, so that the code holds one log2f, not kHL: the
+            // batch-40 call 30.4-31.1 vs 32.6 us on GB300 (two boxes; in 32-head
+            // CTAs the same change measured slower: 128-head call 2.27 vs 2.07 ms)
+            if (w.wq == 0 && (w.lane & 15) < kHL) {
+                const int j = w.lane & 7;
+                float mj = m[0];
+#pragma unroll
+                for (int jj = 1; jj < kHL; ++jj)
+                    if (jj == j) mj = m[jj];
+                float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
+                if (w.hb + j < nrows) {
+                    const float v = (mj + log2f(Lmine[0]) + lse_off) * kLn2;
+                    if (sg.part < 0) dst[w.hb + j] = v;
+                    else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
+                }
+            }
+        } else if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb + kHL - 1
             float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
 #pragma unroll
             for (int j = 0; j < kHL; ++j)
