@@ -1123,9 +1123,6 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
             Lmine[j] = lsum[h] + lsum[G + h] + lsum[2 * G + h] + lsum[3 * G + h] + (coef[h] - coef[h]);
         }
         wg_bar(w.wg);                               // lsum is reused by the next segment; invs is written
-        const int jl = i - 1;                       // the segment's last tile
-        bwait<G>(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
-        fence_after_sync();
         // output rows row0 .. row0 + nrows - 1; a partial slot holds
         // p.part_rows rows, this CTA's from prow0
         int64_t row0;
@@ -1141,6 +1138,28 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
         }
         // o and l are both in units of p * kPScale; lse = m + log2(sum p)
         const float lse_off = -kTau;                 // kPScale = 2^kTau
+        if constexpr (G == 16) {
+            // one lane per head, so that the code holds one log2f, not kHL: the
+            // batch-40 call 30.4-31.1 vs 32.6 us on GB300 (two boxes; in 32-head
+            // CTAs the same change measured slower: 128-head call 2.27 vs 2.07 ms);
+            // stored before the wait for the segment's last PV, which it overlaps
+            if (w.wq == 0 && (w.lane & 15) < kHL) {
+                const int j = w.lane & 7;
+                float mj = m[0];
+#pragma unroll
+                for (int jj = 1; jj < kHL; ++jj)
+                    if (jj == j) mj = m[jj];
+                float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
+                if (w.hb + j < nrows) {
+                    const float v = (mj + log2f(Lmine[0]) + lse_off) * kLn2;
+                    if (sg.part < 0) dst[w.hb + j] = v;
+                    else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
+                }
+            }
+        }
+        const int jl = i - 1;                       // the segment's last tile
+        bwait<G>(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
+        fence_after_sync();
         if constexpr (compact_epilogue<G, E>()) {
             // 128-channel block mb, heads h0 + 4 (st & 3) .. + 3 per step
             const int nh = nrows - w.h0 < 16 ? nrows - w.h0 : 16;   // this warpgroup's rows
@@ -1199,32 +1218,17 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
         fence_before_sync();
         mbar_arrive(&w.bars[O_FREE + (k % S::kOBufs)]);   // a later segment may overwrite O
         mbar_arrive(&w.bars[Q_FREE + qs]);
-        if constexpr (G == 16) {
-            // one lane per head, so that the code holds one log2f, not kHL: the
-            // batch-40 call 30.4-31.1 vs 32.6 us on GB300 (two boxes; in 32-head
-            // CTAs the same change measured slower: 128-head call 2.27 vs 2.07 ms)
-            if (w.wq == 0 && (w.lane & 15) < kHL) {
-                const int j = w.lane & 7;
-                float mj = m[0];
-#pragma unroll
-                for (int jj = 1; jj < kHL; ++jj)
-                    if (jj == j) mj = m[jj];
+        if constexpr (G != 16) {
+            if (w.wq == 0 && (w.lane & 15) == 0) {    // lanes 0 and 16: heads hb .. hb + kHL - 1
                 float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
-                if (w.hb + j < nrows) {
-                    const float v = (mj + log2f(Lmine[0]) + lse_off) * kLn2;
-                    if (sg.part < 0) dst[w.hb + j] = v;
-                    else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
-                }
-            }
-        } else if (w.wq == 0 && (w.lane & 15) == 0) {     // lanes 0 and 16: heads hb .. hb + kHL - 1
-            float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
 #pragma unroll
-            for (int j = 0; j < kHL; ++j)
-                if (w.hb + j < nrows) {
-                    const float v = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
-                    if (sg.part < 0) dst[w.hb + j] = v;
-                    else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
-                }
+                for (int j = 0; j < kHL; ++j)
+                    if (w.hb + j < nrows) {
+                        const float v = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
+                        if (sg.part < 0) dst[w.hb + j] = v;
+                        else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
+                    }
+            }
         }
         ++k;
     }
