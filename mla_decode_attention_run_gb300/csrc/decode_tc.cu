@@ -1157,6 +1157,22 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
                 }
             }
         }
+        if constexpr (G != 16 && !E) {
+            // 32-head decode: lanes 0 and 16 store heads hb .. hb + kHL - 1, also
+            // before the wait (128-head call 2.05 vs 2.07 ms on GB300; one lane
+            // per head measured 2.34).  32-head extend stores after the O: before
+            // the wait it took 689 vs 652 us for the 256-token extend.
+            if (w.wq == 0 && (w.lane & 15) == 0) {
+                float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
+#pragma unroll
+                for (int j = 0; j < kHL; ++j)
+                    if (w.hb + j < nrows) {
+                        const float v = (m[j] + log2f(Lmine[j]) + lse_off) * kLn2;
+                        if (sg.part < 0) dst[w.hb + j] = v;
+                        else st_f32_hint(dst + w.hb + j, v, l2_policy(true));
+                    }
+            }
+        }
         const int jl = i - 1;                       // the segment's last tile
         bwait<G>(&w.bars[PV_DONE + (jl & 1)], (static_cast<uint32_t>(jl) >> 1) & 1, w.abort, w.flags);
         fence_after_sync();
@@ -1218,7 +1234,7 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
         fence_before_sync();
         mbar_arrive(&w.bars[O_FREE + (k % S::kOBufs)]);   // a later segment may overwrite O
         mbar_arrive(&w.bars[Q_FREE + qs]);
-        if constexpr (G != 16) {
+        if constexpr (G != 16 && E) {
             if (w.wq == 0 && (w.lane & 15) == 0) {    // lanes 0 and 16: heads hb .. hb + kHL - 1
                 float* dst = sg.part < 0 ? p.lse + row0 : p.part_lse + int64_t(sg.part) * p.part_rows + prow0;
 #pragma unroll
