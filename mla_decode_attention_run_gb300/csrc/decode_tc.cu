@@ -1199,6 +1199,42 @@ __device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<
                     else st_f32_hint(p.part_o + off + u * kDCkv, o, l2_policy(true));
                 }
             }
+        } else if constexpr (G == 16) {
+            // the next block's TMEM loads go out before this block's stores,
+            // so that the stores cover their latency
+            uint32_t r[2][16];
+            tmem_ld16(w.tmem_lane + ocol + w.h0, r[0]);
+            tmem_ld16(w.tmem_lane + ocol + G + w.h0, r[1]);
+            tmem_wait_ld();
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb) {
+                float o[16];                        // heads h0 .. h0 + 15
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    o[t] = fmaf(__uint_as_float(r[1][t]), 1.f / kP2Scale, __uint_as_float(r[0][t]));
+                if (mb + 1 < 4) {
+                    tmem_ld16(w.tmem_lane + ocol + S::kN * (mb + 1) + w.h0, r[0]);
+                    tmem_ld16(w.tmem_lane + ocol + S::kN * (mb + 1) + G + w.h0, r[1]);
+                }
+                const int ch = mb * 128 + w.row;
+                if (sg.part < 0) {
+                    uint16_t* out = p.out + (int64_t(row0) + w.h0) * kDCkv + ch;
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        if (w.h0 + t >= nrows) break;
+                        out[t * kDCkv] = __bfloat16_as_ushort(__float2bfloat16_rn(o[t] * invs[t]));
+                    }
+                } else {
+                    float* po = p.part_o + (int64_t(sg.part) * p.part_rows + prow0 + w.h0) * kDCkv + ch;
+                    const uint64_t keep = l2_policy(true);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        if (w.h0 + t >= nrows) break;
+                        st_f32_hint(po + t * kDCkv, o[t] * invs[t], keep);
+                    }
+                }
+                if (mb + 1 < 4) tmem_wait_ld();
+            }
         } else {
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
