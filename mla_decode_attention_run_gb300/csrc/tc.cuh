@@ -290,8 +290,11 @@ MLA_DEVINLINE bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort
 // by a hint (0.5, 2 or 8 us) and 37.1 with a bounded try_wait as the first
 // test.
 constexpr uint64_t kPollLimitNs = 1000000;
-MLA_DEVINLINE bool mbar_wait_polled(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags) {
-    if (mbar_test_wait(bar, parity)) return true;
+// The part of the polled wait after a first test found the phase incomplete,
+// out of line: one copy of the loop for every wait site (the 16-head decode
+// kernel 77.4 -> 72.1 KB of code; the batch-40 call 30.66 vs 30.84 us on GB300).
+static __device__ __noinline__ bool mbar_wait_polled_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                         uint32_t* flags) {
     const uint64_t lim = c_wait_limit_ns;
     const uint64_t t0 = global_ns();
     const bool poll = lim < kPollLimitNs;
@@ -304,6 +307,10 @@ MLA_DEVINLINE bool mbar_wait_polled(uint64_t* bar, uint32_t parity, volatile int
             return false;
         }
     }
+}
+MLA_DEVINLINE bool mbar_wait_polled(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* flags) {
+    if (mbar_test_wait(bar, parity)) return true;
+    return mbar_wait_polled_slow(bar, parity, abort, flags);
 }
 
 }  // namespace tc
