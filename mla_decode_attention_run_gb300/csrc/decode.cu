@@ -527,6 +527,7 @@ mla_status_t run_plan(mla_plan_t plan, bool extend, const void* q, int64_t q_str
     p.indices = kv_indices_dev;
     p.seq_lens = seq_lens_dev;
     p.page_size = s.page_size;
+    set_page_divider(p);
     p.heads = s.heads;
     p.head_groups = s.head_groups;
     p.k_scale = k_scale;

@@ -18,6 +18,10 @@ struct DecodeParams {
     const int32_t* indices;
     const int32_t* seq_lens;
     int32_t page_size, heads, head_groups;
+    // t / page_size == (t * page_magic) >> page_shift for 0 <= t < 2^31
+    // (set_page_divider)
+    uint32_t page_magic;
+    int32_t page_shift;
     float k_scale, softmax_scale;
     uint16_t* out;              // BF16 [B][H][512]
     float* lse;                 // [B][H], natural log
@@ -38,6 +42,19 @@ struct DecodeParams {
     const int32_t* blocks;
     int32_t n_blocks;
 };
+
+// Division by the page size as a multiply and a shift, exact for every
+// dividend 0 <= t < 2^31 (the round-up method of Granlund and Montgomery,
+// "Division by Invariant Integers using Multiplication"): with 2^s >= d,
+// m = floor(2^(31+s) / d) + 1 gives 2^(31+s) < m d <= 2^(31+s) + 2^s, so
+// floor(t m / 2^(31+s)) = floor(t / d); m < 2^32 and t m < 2^63.
+inline void set_page_divider(DecodeParams& p) {
+    const uint64_t d = static_cast<uint64_t>(p.page_size > 0 ? p.page_size : 1);
+    int s = 0;
+    while ((uint64_t(1) << s) < d) ++s;
+    p.page_magic = static_cast<uint32_t>((uint64_t(1) << (31 + s)) / d + 1);
+    p.page_shift = 31 + s;
+}
 
 // The tcgen05 decode's token ranges (its CTAs, per head group), passed by
 // value as a kernel parameter: a CTA then knows its segments and issues its

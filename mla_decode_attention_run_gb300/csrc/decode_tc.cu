@@ -299,6 +299,11 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
     return __all_sync(0xffffffffu, bwait<G>(bar, parity, abort, flags));
 }
 
+// The page holding token t (t / page_size by the launch's multiply and shift).
+__device__ __forceinline__ int32_t page_of(const DecodeParams& p, int32_t t) {
+    return static_cast<int32_t>((static_cast<uint64_t>(static_cast<uint32_t>(t)) * p.page_magic) >> p.page_shift);
+}
+
 // Cursor over the tiles of a CTA's segments, with the raw page entries of
 // rows 2 lane, 2 lane + 1 of one tile.
 template <bool E, int N>
@@ -357,15 +362,14 @@ struct TileCursor {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             t[q] = sg.t0 + it * kTT + 2 * lane + q;
-            pg[q] = t[q] < sg.t1 ? pages[p.page_size == 1 ? t[q] : t[q] / p.page_size] : kNoRow;
+            pg[q] = t[q] < sg.t1 ? pages[page_of(p, t[q])] : kNoRow;
         }
     }
     // slot of each row, or -1 (past the context or outside the pool: flagged)
     __device__ void rows(const DecodeParams& p, int32_t (&slot)[2]) const {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const int64_t s = p.page_size == 1 ? int64_t(pg[q])
-                                               : int64_t(pg[q]) * p.page_size + t[q] % p.page_size;
+            const int64_t s = int64_t(pg[q]) * p.page_size + (t[q] - page_of(p, t[q]) * p.page_size);
             const bool ok = pg[q] >= 0 && s < p.num_slots;
             if (!ok && pg[q] != kNoRow) raise_flag(p.flags, MLA_FLAG_INDEX_OOB);
             slot[q] = ok ? static_cast<int32_t>(s) : -1;
