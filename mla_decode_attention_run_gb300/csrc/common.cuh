@@ -178,7 +178,9 @@ MLA_DEVINLINE float fast_exp2(float x) {
 MLA_DEVINLINE void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 MLA_DEVINLINE void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
-MLA_DEVINLINE void raise_flag(uint32_t* flags, uint32_t bit) {
+// Out of line: it runs only on an error, and each inlined copy of the atomic
+// costs code in the paths that call it.
+static __device__ __noinline__ void raise_flag(uint32_t* flags, uint32_t bit) {
     if (flags) atomicOr(flags, bit);
 }
 
