@@ -58,9 +58,11 @@
 //              zero-filled.  Measured on GB300, four LSU warps fed from L2
 //              gather at the HBM rate, which neither fewer warps nor TMA
 //              tile::gather4 reach;
-//   warp 4     one thread issues the QK^T MMAs, tile after tile;
-//   warp 10 [6]  one thread issues the PV MMAs, so that PV of one tile never
-//              waits behind QK^T of the next;
+//   warp 4     issues the QK^T MMAs, tile after tile (G = 16: the whole
+//              warp runs the loop and one elected lane issues; G = 32: one
+//              thread);
+//   warp 10 [6]  issues the PV MMAs the same way, so that PV of one tile
+//              never waits behind QK^T of the next;
 //   warp 5     fetches each segment's [q1;q2;q3] image, per-row score
 //              multipliers and causal limits, written by the q split kernel
 //              that precedes this one (double-buffered for G = 16);
@@ -73,6 +75,10 @@
 //              channel).
 // Every mbarrier wait is bounded; on a timeout the CTA sets
 // MLA_FLAG_WAIT_TIMEOUT, drains its MMAs and copies, frees TMEM and exits.
+// The 16-head and 32-head instantiations differ in several of these forms
+// (issue, waits, epilogue), each chosen by measurement on GB300: the code a
+// CTA runs cold at a segment's end and the instruction cache it shares with
+// the other roles turned out to set much of the call's time.
 #include <mutex>
 #include <vector>
 
@@ -176,7 +182,7 @@ constexpr int kOffFlag = kOffCoef + 2 * 16 * kCoefBytesPerRow;   // rescale vote
 constexpr int kOffMisc = kOffFlag + 64;     // TMEM base, abort flag
 constexpr int kSegTab = 64;                 // segment records a CTA keeps in shared memory
 constexpr int kOffSegTab = kOffMisc + 16;   // kSegTab x 32 B
-constexpr int kOffInv = kOffSegTab + kSegTab * 32;   // compact epilogue: per warpgroup 16 inverse denominators
+constexpr int kOffInv = kOffSegTab + kSegTab * 32;   // epilogue: per warpgroup 16 inverse denominators
 constexpr int kSmemBytes = kOffInv + kMaxG * 4 + 1024;
 static_assert(Shape<16>::kQBufs * 16 * kCoefBytesPerRow <= 2 * 16 * kCoefBytesPerRow &&
                   Shape<32>::kQBufs * 32 * kCoefBytesPerRow <= 2 * 16 * kCoefBytesPerRow,
