@@ -235,6 +235,22 @@ __device__ __forceinline__ Seg load_seg(const DecodeParams& p, int si) {
     return s;
 }
 
+// The same read out of line, for the segments past a 16-head CTA's table
+// (rarely reached; the tables it reads come by value so that no thread copies
+// the launch parameters to local memory for the call).
+template <bool E>
+__device__ __noinline__ Seg load_seg_past_table(const int32_t* segs, const int32_t* blocks, const int32_t* seq_lens,
+                                                int si) {
+    Seg s;
+    s.b = segs[4 * si];
+    s.t0 = segs[4 * si + 1];
+    s.t1 = segs[4 * si + 2];
+    s.part = segs[4 * si + 3];
+    s.req = E ? blocks[4 * s.b] : s.b;
+    s.ntiles = s.t1 <= seq_lens[s.req] ? (s.t1 - s.t0 + kTT - 1) / kTT : 0;
+    return s;
+}
+
 // The CTA's segments lo .. hi - 1.  The first N of them are loaded into
 // shared memory once, before the roles start, so that no role waits on the
 // plan's dependent loads (record, then context length) at a switch between
@@ -249,6 +265,7 @@ struct SegView {
     __device__ __forceinline__ Seg at(const DecodeParams& p, int si) const {
         if constexpr (N > 0) {
             if (si - lo < N) return tab[si - lo].s;
+            return load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si);
         }
         return load_seg<E>(p, si);
     }
@@ -353,7 +370,8 @@ struct TileCursor {
                 pages = p.indices + e.pages;
             } else {
                 pages = p.indices + p.seg_pages[si];
-                sg = load_seg<E>(p, si);
+                sg = N > 0 && sv.tab != nullptr ? load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si)
+                                                : load_seg<E>(p, si);
             }
             it = 0;
             prefetch(p, lane);
