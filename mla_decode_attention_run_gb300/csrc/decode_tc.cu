@@ -266,13 +266,20 @@ struct SegView {
         if constexpr (N > 0) {
             if (si - lo < N) return tab[si - lo].s;
             return load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si);
+        } else if constexpr (N < 0) {
+            return load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si);
         }
         return load_seg<E>(p, si);
     }
 };
 
-template <int G>
-constexpr int seg_tab_entries() { return G == 16 ? kSegTab : 0; }
+// Segment records a CTA keeps in shared memory: 16-head CTAs kSegTab; 32-head
+// CTAs none, and 32-head decode CTAs (-1) read each record through one
+// out-of-line call (128-head call 2.03 vs 2.07 ms on GB300; 32-head extend
+// keeps the inlined read: out of line it measured 661 vs 636 us for the
+// 256-token extend, and 16-head decode 30.30 vs 30.15 us).
+template <int G, bool E>
+constexpr int seg_tab_entries() { return G == 16 ? kSegTab : (E ? 0 : -1); }
 
 template <bool E, int N>
 __device__ __forceinline__ int count_tiles(const DecodeParams& p, const SegView<E, N>& sv) {
@@ -351,7 +358,7 @@ struct TileCursor {
             sg.t1 = first->y;
             it = 0;
             prefetch(p, lane);
-            sg = load_seg<E>(p, si);
+            sg = N < 0 ? load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si) : load_seg<E>(p, si);
             if (sg.ntiles > 0) return;
             ++si;
         }
@@ -370,8 +377,8 @@ struct TileCursor {
                 pages = p.indices + e.pages;
             } else {
                 pages = p.indices + p.seg_pages[si];
-                sg = N > 0 && sv.tab != nullptr ? load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si)
-                                                : load_seg<E>(p, si);
+                sg = (N > 0 && sv.tab != nullptr) || N < 0 ? load_seg_past_table<E>(p.segs, p.blocks, p.seq_lens, si)
+                                                           : load_seg<E>(p, si);
             }
             it = 0;
             prefetch(p, lane);
@@ -605,7 +612,7 @@ __device__ __forceinline__ bool issuer_wait(uint64_t* bar, uint32_t parity, cons
 }
 
 template <int G, bool E>
-__device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<E, seg_tab_entries<G>()>& sv) {
+__device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<E, seg_tab_entries<G, E>()>& sv) {
     using S = Shape<G>;
     int total = 0;
     for (int si = sv.lo; si < sv.hi; ++si) {
@@ -614,7 +621,7 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<
             raise_flag(p.flags, MLA_FLAG_PLAN_MISMATCH);
         total += sg.ntiles;
     }
-    SegWalk<E, seg_tab_entries<G>()> wq;
+    SegWalk<E, seg_tab_entries<G, E>()> wq;
     wq.init(p, sv);
     for (int qk = 0; qk < total; ++qk) {
         const int slot = qk & 1;
@@ -636,10 +643,10 @@ __device__ void qk_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<
 }
 
 template <int G, bool E>
-__device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<E, seg_tab_entries<G>()>& sv) {
+__device__ void pv_issuer(const DecodeParams& p, const MmaCtx& c, const SegView<E, seg_tab_entries<G, E>()>& sv) {
     using S = Shape<G>;
     const int total = count_tiles<E>(p, sv);
-    SegWalk<E, seg_tab_entries<G>()> wp;
+    SegWalk<E, seg_tab_entries<G, E>()> wp;
     wp.init(p, sv);
     for (int pv = 0; pv < total; ++pv) {
         const int ob = wp.k % S::kOBufs;
@@ -840,7 +847,7 @@ __global__ void __maxnreg__(56) mla_q_split_kernel(const DecodeParams p) {
 // multipliers) once the split kernel has finished.
 template <int G, bool E>
 __device__ void q_fetch(const DecodeParams& p, uint8_t* base, uint64_t* bars, volatile int* abort,
-                        const SegView<E, seg_tab_entries<G>()>& sv, int lane) {
+                        const SegView<E, seg_tab_entries<G, E>()>& sv, int lane) {
     using S = Shape<G>;
     if (lane != 0) return;
     griddep_wait();                                 // the q images are complete
@@ -952,7 +959,7 @@ template <int V>
 __device__ __forceinline__ bool half_reduce_writer(int lane) { return V == 16 || (lane & 1) == 0; }
 
 template <int G, bool E>
-__device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<E, seg_tab_entries<G>()>& sv,
+__device__ void softmax_wg(const DecodeParams& p, const WgCtx& w, const SegView<E, seg_tab_entries<G, E>()>& sv,
                            int head0) {
     using S = Shape<G>;
     constexpr int kHL = 8;                          // heads per lane
@@ -1333,7 +1340,7 @@ __global__ void __maxnreg__(G == 16 ? 152 : 128)
     const int seg_lo = ranged ? ranges.seg[blockIdx.x] : p.cta_ptr[blockIdx.x];
     const int seg_hi = ranged ? ranges.seg[blockIdx.x + 1] : p.cta_ptr[blockIdx.x + 1];
     // the segment table: one thread per segment, visible after the barrier below
-    constexpr int kTab = seg_tab_entries<G>();
+    constexpr int kTab = seg_tab_entries<G, E>();
     SegEntry* segtab = reinterpret_cast<SegEntry*>(base + kOffSegTab);
     if (tid < kTab && seg_lo + tid < seg_hi)
         segtab[tid] = SegEntry{load_seg<E>(p, seg_lo + tid), p.seg_pages[seg_lo + tid], 0};
