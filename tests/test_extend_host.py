@@ -12,6 +12,7 @@ import mla_decode_attention_run_gb300 as M
 
 QIMAGE_BYTES = 3 * 16 * 576 + 16 * 12      # [q1;q2;q3] rows + two multipliers and a limit per row
 TILE = 64
+EXTEND_SEGMENT_COST = 4   # tiles' worth of CTA time the extend schedule charges per segment
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -80,6 +81,29 @@ def _check(lens, q_lens, heads, ps=1, num_sms=152):
 ])
 def test_extend_schedule_covers_rows_and_contexts(lens, q_lens, heads, ps):
     _check(lens, q_lens, heads, ps)
+
+
+@pytest.mark.parametrize("lens,q_lens", [
+    ([5000, 1200, 3000, 800], [4, 4, 4, 4]),
+    (list(np.random.default_rng(3).integers(1024, 8193, 40)), [4] * 40),   # speculative, batch 40
+    ([4000] * 8, [256] * 8),                                              # prefill chunks
+])
+def test_extend_schedule_balances_cost(lens, q_lens):
+    """The largest CTA cost (tiles + a fixed cost per segment) is within one
+    segment of the even share, and with tiles enough every CTA has work (the
+    plan splits the costliest range until none is idle)."""
+    segs, blocks, info = _check(lens, q_lens, 16)
+    ctas = info["num_ctas"]
+    tiles = np.zeros(ctas, np.int64)
+    nseg = np.zeros(ctas, np.int64)
+    for c, _, t0, t1, _ in segs:
+        tiles[c] += (t1 - t0 + TILE - 1) // TILE
+        nseg[c] += 1
+    total = int(tiles.sum()) + EXTEND_SEGMENT_COST * blocks.shape[0]
+    cost = tiles + EXTEND_SEGMENT_COST * nseg
+    assert cost.max() <= -(-total // ctas) + EXTEND_SEGMENT_COST + 1
+    if tiles.sum() >= 152:
+        assert ctas == 152 and tiles.min() >= 1
 
 
 def test_one_new_token_per_request_reads_each_whole_context():
