@@ -400,7 +400,10 @@ mla_status_t mla_get_last_error(void* stream, uint32_t* device_flags_out);
  * decode inside CUDA graphs of a serving loop, where a hung kernel stalls
  * every request).  The limit is 2 s; this call sets it, in nanoseconds, for
  * the current device (0 restores 2 s).  A tiny limit makes the next calls
- * give up at their first wait, which is how the timeout path is tested.
+ * give up early, which is how the timeout path is tested: under 1 ms,
+ * 16-head CTAs poll their barriers without suspending and give up at the
+ * first wait that finds its barrier not ready; 32-head CTAs give up at the
+ * first wait that outlasts one suspended try_wait.
  * Synchronous: call it between launches, with no decode kernel running.
  * Errors: MLA_ERR_CUDA.
  */
